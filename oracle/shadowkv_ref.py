@@ -1,0 +1,305 @@
+"""ShadowKV decode-step sparse attention: a plain, slow float64 CPU oracle.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import this module.  The product path
+(the CUDA library and its Python binding) never calls it and shares no code
+with it; both sides take their inputs from ``workload``.
+
+Everything here is numpy in float64 and follows the two algorithms of the
+pages in their order and notation:
+
+* "ShadowKV: KV Cache in Shadows for High-Throughput Long-Context LLM
+  Inference" (Chinese digest, section A2, Algorithm 1 "pre-filling" and
+  Algorithm 2 "decoding"),
+* the English summary of the same paper, section 3.4 ("Landmark Construction
+  and Outlier Detection", "Decoding-Time KV Selection", "Sparse KV
+  Reconstruction", "Theoretical Equivalent Bandwidth Model") and its
+  appendix A.2 memory-savings formula.
+
+Readings where the pages are silent (each is also listed in the design notes):
+
+* RoPE is the Llama/NeoX half-split rotation, theta_i = base^(-2i/d), positions
+  0-based, no frequency scaling.
+* q-head j belongs to KV head j // G (contiguous grouped-query mapping).
+* A is shared by the KV heads of one batch element: A [S][r], B_h [r][d].
+* Outliers are chosen per (batch, KV head) among the chunks outside the local
+  window, by the lowest minimum cosine between each token and its chunk mean;
+  equal values rank the lower chunk id first.
+* The local window (the last W prefill tokens) and every decode token are kept
+  exact and are neither landmarks nor selectable.
+* The softmax of the selection runs over the n_c selectable chunks only.
+* The query and the new key arrive post-RoPE at position S+t.
+
+Parity pins: see ``tests/test_oracle_pins.py`` and ``tests/test_golden.py``.
+The selection scores' near-tie band is not pinned by the pages (no page prints
+per-element outputs); nothing here is "parity unpinned" beyond that.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+# ----------------------------------------------------------------------------
+# RoPE (pages silent on the convention; reading: Llama half-split)
+# ----------------------------------------------------------------------------
+
+
+def rope_theta(d: int, base: float) -> np.ndarray:
+    """theta_i = base^(-2i/d) for i < d/2, in float64."""
+    i = np.arange(d // 2, dtype=np.float64)
+    return np.power(float(base), -2.0 * i / d)
+
+
+def apply_rope(x: np.ndarray, pos: np.ndarray, base: float) -> np.ndarray:
+    """Rotate rows x [n][d] at integer positions pos [n] (half-split pairs i, i+d/2)."""
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    h = d // 2
+    ang = np.asarray(pos, dtype=np.float64)[:, None] * rope_theta(d, base)[None, :]
+    c, s = np.cos(ang), np.sin(ang)
+    x1, x2 = x[:, :h], x[:, h:]
+    return np.concatenate([x1 * c - x2 * s, x1 * s + x2 * c], axis=1)
+
+
+def rebuild_keys(A_rows: np.ndarray, B_h: np.ndarray, pos: np.ndarray, base: float) -> np.ndarray:
+    """Post-RoPE keys of the given tokens from the low-rank factors.
+
+    Summary page, section 3.4 "Sparse KV Reconstruction": K_sparse =
+    MatMul(Gather(A, I), B), then RoPE at the tokens' own positions.
+    """
+    return apply_rope(np.asarray(A_rows, np.float64) @ np.asarray(B_h, np.float64), pos, base)
+
+
+def chunk_tokens(chunk_ids, C: int) -> np.ndarray:
+    """Token positions of the given chunks, chunk by chunk."""
+    ids = np.asarray(chunk_ids, dtype=np.int64)
+    return (ids[:, None] * C + np.arange(C, dtype=np.int64)[None, :]).reshape(-1)
+
+
+# ----------------------------------------------------------------------------
+# Algorithm 1 (pre-filling)
+# ----------------------------------------------------------------------------
+
+
+def reduce_chunks(K_rope: np.ndarray, C: int) -> np.ndarray:
+    """Landmark of chunk j: the mean of its C post-RoPE keys (summary page,
+    "Landmark Construction": k_bar_j = (1/c) sum_i k_RoPE)."""
+    n = K_rope.shape[0] // C
+    return K_rope[: n * C].reshape(n, C, -1).mean(axis=1)
+
+
+def cosine(x: np.ndarray, y: np.ndarray) -> np.ndarray:
+    """cos(x, y) = x.y / max(|x||y|, 1e-12), row-wise."""
+    num = np.sum(x * y, axis=-1)
+    den = np.linalg.norm(x, axis=-1) * np.linalg.norm(y, axis=-1)
+    return num / np.maximum(den, 1e-12)
+
+
+def chunk_min_cos(K_rope: np.ndarray, L: np.ndarray, C: int) -> np.ndarray:
+    """Min over the chunk's tokens of cos(token key, chunk landmark)
+    (Algorithm 1: S = CosineSimilarity(C, K_RoPE), then Min(S, dim=-1))."""
+    n = L.shape[0]
+    Kc = K_rope[: n * C].reshape(n, C, -1)
+    return cosine(Kc, L[:, None, :]).min(axis=1)
+
+
+def arg_topk(scores: np.ndarray, k: int) -> np.ndarray:
+    """Indices of the k largest scores in rank order; equal scores rank the
+    lower index first (ArgTopK of Algorithms 1 and 2 with a fixed tie rule)."""
+    scores = np.asarray(scores, dtype=np.float64)
+    order = np.lexsort((np.arange(scores.shape[0]), -scores))
+    return order[:k]
+
+
+@dataclass
+class UnitPrefill:
+    """Per (batch, KV head) state that Algorithm 1 leaves on the GPU."""
+    landmarks: np.ndarray      # [n_c][d]   L = C \ Gather(C, I), selectable chunks only
+    ids: np.ndarray            # [n_c]      original chunk id of each landmark (ascending)
+    outlier_ids: np.ndarray    # [O]        ascending
+    min_cos: np.ndarray        # [S/C - W/C] per candidate chunk
+    all_landmarks: np.ndarray  # [S/C - W/C][d]
+    k_outlier: np.ndarray      # [O*C][d]
+    v_outlier: np.ndarray      # [O*C][d]
+    k_local: list = field(default_factory=list)   # rows, W prefill tokens then decode tokens
+    v_local: list = field(default_factory=list)
+
+
+def prefill_unit(A_b, B_bh, V_bh, C: int, O: int, W: int, base: float) -> UnitPrefill:
+    """Algorithm 1 for one (batch, KV head), with the factors A, B given.
+
+    The SVD step is out of scope: A [S][r] and B_h [r][d] are inputs, the
+    pre-RoPE keys are A.B_h and K_RoPE is their rotation at positions 0..S-1.
+    """
+    A_b = np.asarray(A_b, np.float64)
+    V_bh = np.asarray(V_bh, np.float64)
+    S = A_b.shape[0]
+    n_chunk = S // C
+    n_cand = n_chunk - W // C
+    K_rope = rebuild_keys(A_b, B_bh, np.arange(S), base)          # K_RoPE
+    Cm = reduce_chunks(K_rope[: n_cand * C], C)                    # C = Reduce(K_RoPE)
+    mcos = chunk_min_cos(K_rope, Cm, C)                            # Min(CosineSimilarity)
+    out_ids = np.sort(arg_topk(-mcos, O))                          # ArgTopK(-Min(S), o)
+    keep = np.ones(n_cand, dtype=bool)
+    keep[out_ids] = False
+    ids = np.nonzero(keep)[0]
+    tok_o = chunk_tokens(out_ids, C)
+    st = UnitPrefill(landmarks=Cm[ids], ids=ids, outlier_ids=out_ids, min_cos=mcos,
+                     all_landmarks=Cm, k_outlier=K_rope[tok_o], v_outlier=V_bh[tok_o])
+    for p in range(S - W, S):
+        st.k_local.append(K_rope[p])
+        st.v_local.append(V_bh[p])
+    return st
+
+
+# ----------------------------------------------------------------------------
+# Algorithm 2 (decoding)
+# ----------------------------------------------------------------------------
+
+
+def softmax_rows(x: np.ndarray) -> np.ndarray:
+    m = x.max(axis=-1, keepdims=True)
+    e = np.exp(x - m)
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def select_chunks(q_group: np.ndarray, landmarks: np.ndarray, ids: np.ndarray, k: int) -> dict:
+    """Landmark-guided selection for one KV head.
+
+    q_group [G][d] are the post-RoPE queries of the G query heads that share
+    this KV head (s_q = 1).  P = MatMul(Q, L^T); S = Softmax(P / sqrt(d));
+    S1 = sum over query tokens (a no-op for one token); S2 = max over the group;
+    I = ArgTopK(S2, k).  Returns the selected original chunk ids ascending.
+    """
+    q = np.asarray(q_group, np.float64)
+    L = np.asarray(landmarks, np.float64)
+    d = q.shape[-1]
+    P = q @ L.T                              # [G][n_c]
+    S = softmax_rows(P / math.sqrt(d))       # per query head over the n_c chunks
+    S1 = S                                   # sum over s_q = 1 query tokens
+    S2 = S1.max(axis=0)                      # max_kv_group
+    ranked = arg_topk(S2, k)
+    return {"P": P, "S": S, "S2": S2, "ranked": ranked,
+            "sel": np.sort(np.asarray(ids)[ranked])}
+
+
+def hit_miss(prev_sel, cur_sel):
+    """Index scan against the previous step's selection: (hits, misses), each ascending."""
+    cur = np.asarray(cur_sel, dtype=np.int64)
+    if prev_sel is None:
+        return np.zeros(0, np.int64), np.sort(cur)
+    inprev = np.isin(cur, np.asarray(prev_sel, dtype=np.int64))
+    return np.sort(cur[inprev]), np.sort(cur[~inprev])
+
+
+def attend(q_group: np.ndarray, K: np.ndarray, V: np.ndarray) -> np.ndarray:
+    """Exact softmax(q K^T / sqrt(d)) V for each of the G query rows."""
+    q = np.asarray(q_group, np.float64)
+    d = q.shape[-1]
+    s = q @ np.asarray(K, np.float64).T / math.sqrt(d)
+    return softmax_rows(s) @ np.asarray(V, np.float64)
+
+
+def attend_on_index_set(q_group, A_b, B_bh, V_bh, outlier_ids, sel_ids, k_local, v_local,
+                        C: int, base: float) -> np.ndarray:
+    """Attention over [K_outlier; RoPE(K_sparse); K_local] for given index sets
+    (summary page, "Assembly of the final sparse KV cache").  Keys of outlier
+    and selected chunks are rebuilt here in float64 from A and B."""
+    A_b = np.asarray(A_b, np.float64)
+    V_bh = np.asarray(V_bh, np.float64)
+    to = chunk_tokens(outlier_ids, C)
+    ts = chunk_tokens(sel_ids, C)
+    d = np.asarray(B_bh).shape[1]
+    K = np.concatenate([rebuild_keys(A_b[to], B_bh, to, base),
+                        rebuild_keys(A_b[ts], B_bh, ts, base),
+                        np.asarray(k_local, np.float64).reshape(-1, d)])
+    V = np.concatenate([V_bh[to], V_bh[ts], np.asarray(v_local, np.float64).reshape(-1, d)])
+    return attend(q_group, K, V)
+
+
+@dataclass
+class UnitDecodeState:
+    pre: UnitPrefill
+    prev_sel: np.ndarray | None = None
+    steps: int = 0
+
+
+def decode_step_unit(st: UnitDecodeState, q_group, k_new, v_new, A_b, B_bh, V_bh,
+                     k: int, C: int, base: float) -> dict:
+    """One step of Algorithm 2 for one (batch, KV head).
+
+    Appends the new token to the exact local set, selects k chunks, rebuilds
+    their keys, takes their values and attends over outliers + selected
+    chunks + local tokens.  Returns the output [G][d], the selection and the
+    hit/miss split against the previous step.
+    """
+    st.pre.k_local.append(np.asarray(k_new, np.float64))
+    st.pre.v_local.append(np.asarray(v_new, np.float64))
+    sel = select_chunks(q_group, st.pre.landmarks, st.pre.ids, k)
+    hits, misses = hit_miss(st.prev_sel, sel["sel"])
+    A_b = np.asarray(A_b, np.float64)
+    V_bh = np.asarray(V_bh, np.float64)
+    ts = chunk_tokens(sel["sel"], C)
+    K = np.concatenate([st.pre.k_outlier, rebuild_keys(A_b[ts], B_bh, ts, base),
+                        np.stack(st.pre.k_local)])
+    V = np.concatenate([st.pre.v_outlier, V_bh[ts], np.stack(st.pre.v_local)])
+    out = attend(q_group, K, V)
+    st.prev_sel = sel["sel"]
+    st.steps += 1
+    return {"out": out, "sel": sel["sel"], "S2": sel["S2"], "ranked": sel["ranked"],
+            "hits": hits, "misses": misses}
+
+
+# ----------------------------------------------------------------------------
+# Analytical models (summary page section 3.4 and appendix A.2; digest A2)
+# ----------------------------------------------------------------------------
+
+
+def equivalent_bandwidth(S, C, K, O, alpha, B_gpu, B_pcie):
+    """B~ = 2 S B_GPU / (S/C + 2(K+O)C + (1-alpha) K C B_GPU / B_PCIe)."""
+    return 2.0 * S * B_gpu / (S / C + 2.0 * (K + O) * C + (1.0 - alpha) * K * C * B_gpu / B_pcie)
+
+
+def equivalent_bandwidth_terms(S, C, K, O, alpha, B_gpu, B_pcie):
+    """The three denominator terms of the equivalent-bandwidth formula."""
+    return (S / C, 2.0 * (K + O) * C, (1.0 - alpha) * K * C * B_gpu / B_pcie)
+
+
+def memory_savings(S, M, C, K, O, r):
+    """2SM / (SM/C + 2(K+O)C + Sr + rM), taken literally as printed."""
+    return 2.0 * S * M / (S * M / C + 2.0 * (K + O) * C + S * r + r * M)
+
+
+def compression_ratio(s, d, r):
+    """sd / (r(s + d)): storage of A and B against the full key cache."""
+    return s * d / (r * (s + d))
+
+
+def sparse_budget_tokens(K, O, C):
+    """Tokens attended from the context per KV head: (K + O) C."""
+    return (K + O) * C
+
+
+# ----------------------------------------------------------------------------
+# Helpers for comparing with stored low-precision state
+# ----------------------------------------------------------------------------
+
+
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to bfloat16 (nearest even, via float32) and return float64."""
+    f = np.asarray(x, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    u = (u + 0x7FFF + lsb) >> 16 << 16
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def near_tie_band(scores: np.ndarray, k: int, rel: float = 1e-4):
+    """Indices whose score lies within ``rel`` (relative) of the k-th largest
+    score: membership of these may legitimately differ between two correct
+    implementations that round differently."""
+    scores = np.asarray(scores, np.float64)
+    kth = scores[arg_topk(scores, k)[-1]]
+    return np.nonzero(np.abs(scores - kth) <= rel * abs(kth))[0], kth

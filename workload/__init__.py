@@ -1,0 +1,9 @@
+"""Seeded synthetic workloads (sizes and input generators) for the decode path.
+
+This package holds no arithmetic of the method; the CUDA path and the oracle
+both take their inputs from it and share nothing else.
+"""
+from .configs import (ALL, LLAMA_128K, LLAMA_1M, LLAMA_32K, SWEEP_64K, TINY,  # noqa: F401
+                      Workload, sweep_points)
+from .gen import (make_A, make_B, make_decode_inputs, make_layer, make_V,  # noqa: F401
+                  spike_chunks, storage_dtype)
