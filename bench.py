@@ -1,0 +1,428 @@
+"""Decode-step benchmark of the ShadowKV sparse-attention path on GB300.
+
+One step = one decode step of every layer (all rows of the hot path: landmark
+scoring, top-K + index scan + append, key rebuild, value fetch, sparse
+attention) for the whole batch.  Default workload: Llama-3.1-8B attention
+shape at 128K context, batch 8, 32 layers, values in page-locked host memory.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
+of the workload (independent batches, no collective on the data path) and the
+timing is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workload import ALL, LLAMA_128K, Workload  # noqa: E402
+
+METRIC = "sparse decode-attention tokens/s and HBM GB/s (% of 8 TB/s) at 128K, 1×GB300"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default=LLAMA_128K.name, choices=sorted(ALL))
+    ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count")
+    ap.add_argument("--batch", type=int, default=0)
+    ap.add_argument("--v-place", default="", choices=["", "hbm", "host"])
+    ap.add_argument("--drift", type=float, default=-1.0)
+    ap.add_argument("--share-storage", default="auto", choices=["auto", "yes", "no"],
+                    help="reuse one layer's A/B/V for every layer (state stays per layer)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def workload_from(args) -> Workload:
+    w = ALL[args.config]
+    kw = {}
+    if args.layers:
+        kw["layers"] = args.layers
+    if args.batch:
+        kw["batch"] = args.batch
+    if args.v_place:
+        kw["v_place"] = args.v_place
+    if args.drift >= 0:
+        kw["drift"] = args.drift
+    return w.with_(**kw) if kw else w
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def mem_available_gb() -> float:
+    try:
+        for line in open("/proc/meminfo"):
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) / 1e6
+    except OSError:
+        pass
+    return 0.0
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clocks and throttle reasons during a timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu, self.proc, self.path = gpu, None, None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait(timeout=5)
+        rows = [r.split(",") for r in open(self.path).read().strip().splitlines() if r.strip()]
+        os.unlink(self.path)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args, w: Workload, ws: int, rank: int, local: int):
+    import torch
+    import torch.distributed as dist
+
+    import sparse_kv_cache_gb300 as skv
+    from workload import make_A, make_B, make_decode_inputs, make_V, storage_dtype
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    K, W = args.steps, args.warmup
+    passes = 3
+    total_steps = W + passes * K
+    w = w.with_(seed=w.seed + 1000 * rank, steps=total_steps)
+    L = w.layers
+    dt = storage_dtype(w)
+    es = 2 if w.dtype == "bf16" else 4
+    v_bytes = w.batch * w.n_kv_heads * w.seq_len * w.head_dim * es
+    share = args.share_storage == "yes"
+    if args.share_storage == "auto" and w.v_place == "host":
+        share = mem_available_gb() < 1.3 * L * v_bytes / 1e9 + 16
+    n_data = 1 if share else L
+
+    main = torch.cuda.Stream(dev)
+    side = torch.cuda.Stream(dev)
+    data, layers = [], []
+    t0 = time.time()
+    for ell in range(n_data):
+        A = make_A(w, ell, dev)
+        B = make_B(w, ell, dev)
+        Vd = make_V(w, ell, dev)
+        if w.v_place == "host":
+            Vh = torch.empty(Vd.shape, dtype=dt, pin_memory=True)
+            Vh.copy_(Vd)
+            del Vd
+            V = Vh
+        else:
+            V = Vd
+        data.append((A, B, V))
+    cfg = skv.make_config(w, max_new_tokens=total_steps)
+    for ell in range(L):
+        A, B, V = data[ell % n_data]
+        layers.append(skv.Layer(cfg, A, B, V, stream=main))
+    torch.cuda.synchronize()
+    setup_s = time.time() - t0
+    # per-layer decode inputs for every step, resident in HBM
+    qs, kns, vns = [], [], []
+    for ell in range(L):
+        q, kn, vn = make_decode_inputs(w, ell, total_steps, dev)
+        qs.append(q); kns.append(kn); vns.append(vn)
+    out = [torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=dt, device=dev) for _ in range(L)]
+    hq = [lay.handle for lay in layers]
+    lib = skv.load()
+    ms_, ss_ = main.cuda_stream, side.cuda_stream
+
+    def step(s: int):
+        for ell in range(L):
+            rc = lib.shadowkv_decode_step(hq[ell], qs[ell][s].data_ptr(), kns[ell][s].data_ptr(),
+                                          vns[ell][s].data_ptr(), out[ell].data_ptr(), None, ms_, ss_)
+            if rc:
+                raise skv.ShadowKVError(rc, "decode_step")
+
+    def barrier():
+        torch.cuda.synchronize()
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x: float) -> float:
+        if ws == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    s_idx = 0
+    for _ in range(W):
+        step(s_idx); s_idx += 1
+    for lay in layers:
+        lay.reset_stats()
+
+    # ---- pass 1: device-resident inputs (the headline value)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(main)
+    for _ in range(K):
+        step(s_idx); s_idx += 1
+    e1.record(main)
+    barrier()
+    clk = clocks.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1))
+    st = [lay.stats() for lay in layers]
+    hbm = sum(s["hbm_bytes"] for s in st)
+    link = sum(s["link_bytes"] for s in st)
+    scratch = sum(s["scratch_bytes"] for s in st)
+    alpha = statistics.mean(s["alpha_mean"] for s in st)
+
+    # ---- pass 2: the same steps with per-phase CUDA events (roofline of the dominant kernel)
+    for lay in layers:
+        lay.reset_stats()
+        lay.set_profiling(True)
+    barrier()
+    for _ in range(K):
+        step(s_idx); s_idx += 1
+    barrier()
+    st2 = [lay.stats() for lay in layers]
+    for lay in layers:
+        lay.set_profiling(False)
+    phase_ms = {ph: sum(s["phase_ms"][ph] for s in st2) for ph in skv.PHASES}
+    phase_n = {ph: sum(s["phase_launches"][ph] for s in st2) for ph in skv.PHASES}
+    score_us = 1000.0 * phase_ms["score"] / max(1, phase_n["score"])
+    score_bytes = w.units * (w.n_selectable + w.group) * w.head_dim * es   # landmarks + queries
+    achieved = score_bytes / (score_us * 1e-6) / 1e9
+    peak, peak_kind = measured_peaks()
+
+    # ---- pass 3: end to end through the public call with host buffers
+    e2e = None
+    if not args.no_e2e:
+        qh = [qs[ell][s_idx:s_idx + K].to("cpu").pin_memory() for ell in range(L)]
+        kh = [kns[ell][s_idx:s_idx + K].to("cpu").pin_memory() for ell in range(L)]
+        vh = [vns[ell][s_idx:s_idx + K].to("cpu").pin_memory() for ell in range(L)]
+        oh = torch.empty((K, L) + tuple(out[0].shape), dtype=dt, pin_memory=True)
+        qd = [torch.empty_like(qs[ell][0]) for ell in range(L)]
+        kd = [torch.empty_like(kns[ell][0]) for ell in range(L)]
+        vd = [torch.empty_like(vns[ell][0]) for ell in range(L)]
+        barrier()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(main):
+            f0.record(main)
+            for k in range(K):
+                for ell in range(L):
+                    qd[ell].copy_(qh[ell][k], non_blocking=True)
+                    kd[ell].copy_(kh[ell][k], non_blocking=True)
+                    vd[ell].copy_(vh[ell][k], non_blocking=True)
+                    layers[ell].decode_step(qd[ell], kd[ell], vd[ell], out[ell], None, main=main, side=side)
+                    oh[k, ell].copy_(out[ell], non_blocking=True)
+            f1.record(main)
+        barrier()
+        ms_e2e = max_over_ranks(f0.elapsed_time(f1))
+        h2d = L * (qd[0].numel() + kd[0].numel() + vd[0].numel()) * es
+        d2h = L * out[0].numel() * es
+        e2e = {"value": ws * w.batch * K / (ms_e2e / 1000.0), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        s_idx += K
+
+    st_all = [lay.stats(check=False) for lay in layers]
+    dev_err = [s["device_error"] for s in st_all if s["device_error"]]
+    for lay in layers:
+        lay.close()
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return None
+
+    tokens_s = ws * w.batch * K / (ms / 1000.0)
+    step_ms = ms / K
+    hbm_per_step = hbm / K
+    line = {
+        "metric": METRIC, "value": tokens_s, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": W,
+        "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic (seeded generator; Llama-3.1-8B attention shape)",
+        "config": {"workload": w.name, "layers": L, "batch_per_gpu": w.batch, "seq_len": w.seq_len,
+                   "n_kv_heads": w.n_kv_heads, "n_q_heads": w.n_q_heads, "head_dim": w.head_dim,
+                   "rank": w.rank, "chunk": w.chunk, "n_select": w.n_select, "n_outlier": w.n_outlier,
+                   "local_window": w.local_window, "v_place": w.v_place, "drift": w.drift,
+                   "parallelism": f"replicas x{ws} (batch sharded, no collective)",
+                   "layers_share_input_storage": share,
+                   "l2": "inputs larger than L2 (landmarks of one layer exceed 129 MB)"},
+        "hbm_gbs": hbm_per_step / (step_ms * 1e-3) / 1e9,
+        "hbm_frac_of_8tbs": hbm_per_step / 8e12 / (step_ms * 1e-3),
+        "hbm_bytes_per_step": hbm_per_step, "link_bytes_per_step": link / K,
+        "link_gbs": (link / K) / (step_ms * 1e-3) / 1e9, "scratch_bytes_per_step": scratch / K,
+        "alpha_mean": alpha,
+        "roofline": {"bound": "hbm", "kernel": "k_score (landmark scoring)", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": peak_kind, "traffic": None,
+                     "algorithmic_bytes_per_launch": score_bytes, "avg_launch_us": score_us},
+        "phase_ms_per_step": {ph: phase_ms[ph] / K for ph in skv.PHASES},
+        "clocks": clk,
+        "e2e": e2e,
+        "gpu_launches": 5 * L * K,
+        "setup_s": setup_s,
+    }
+    if dev_err:
+        line["device_error"] = dev_err[0]
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, seconds=12.0)
+    if ws > 1:
+        dist.destroy_process_group()
+    return line
+
+
+# ----------------------------------------------------------------------------- oracle arm
+class OracleSample:
+    """The float64 oracle's decode step on one (batch, KV head) unit of layer 0,
+    on this host's cores.  Inputs of that unit come from the same seeded
+    generator (CPU stream); the oracle's pre-filling of the unit is untimed."""
+
+    def __init__(self, w: Workload, unit: int = 0, max_steps: int = 4096):
+        from oracle import shadowkv_ref as ref
+        from workload import make_A, make_B, make_decode_inputs, make_V
+        self.ref, self.w = ref, w
+        b, h = divmod(unit, w.n_kv_heads)
+        one = w.with_(batch=b + 1)
+        self.A = make_A(one, 0, "cpu")[b].double().numpy()
+        self.B = make_B(one, 0, "cpu")[b, h].double().numpy()
+        self.V = make_V(one.with_(n_kv_heads=h + 1), 0, "cpu")[b, h].double().numpy()
+        q, kn, vn = make_decode_inputs(one, 0, min(max_steps, 256), "cpu")
+        G = w.group
+        self.q = q[:, b, h * G:(h + 1) * G].double().numpy()
+        self.kn, self.vn = kn[:, b, h].double().numpy(), vn[:, b, h].double().numpy()
+        t0 = time.perf_counter()
+        self.st = ref.UnitDecodeState(ref.prefill_unit(self.A, self.B, self.V, w.chunk, w.n_outlier,
+                                                       w.local_window, w.rope_base))
+        self.prefill_s = time.perf_counter() - t0
+        self.t = 0
+
+    def timed_steps(self, budget_s: float, cap: int = 1 << 30):
+        """Run unit-steps until ``budget_s`` of oracle time; returns (seconds per unit-step, n)."""
+        w, ref = self.w, self.ref
+        timed, n = 0.0, 0
+        while n < cap and (n == 0 or timed < budget_s):
+            t = self.t % self.q.shape[0]
+            if self.st.steps >= self.q.shape[0]:
+                self.st.pre.k_local = self.st.pre.k_local[: w.local_window]
+                self.st.pre.v_local = self.st.pre.v_local[: w.local_window]
+                self.st.steps = 0
+            t1 = time.perf_counter()
+            ref.decode_step_unit(self.st, self.q[t], self.kn[t], self.vn[t], self.A, self.B, self.V,
+                                 w.n_select, w.chunk, w.rope_base)
+            timed += time.perf_counter() - t1
+            n += 1
+            self.t += 1
+        return timed / n, n
+
+
+def cpu_baseline(w: Workload, seconds: float = 12.0) -> dict:
+    o = OracleSample(w)
+    per_unit, n = o.timed_steps(seconds)
+    step_s = per_unit * w.units * w.layers
+    return {"value": w.batch / step_s, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": (f"{n} oracle decode steps of one (batch, KV head) unit of layer 0 ({per_unit * 1e3:.1f} ms "
+                       f"each), scaled to {w.units} units x {w.layers} layers per decode step; the unit's "
+                       f"oracle pre-filling ({o.prefill_s:.1f} s) untimed; numpy BLAS may use every host core")}
+
+
+def run_reference(args, w: Workload, ws: int, rank: int):
+    if rank != 0:
+        return None
+    K, W = args.steps, args.warmup
+    budget = max(0.5, min(10.0, 120.0 / max(1, K + W)))
+    o = OracleSample(w)
+    for _ in range(W):
+        o.timed_steps(budget / 4, cap=2)
+    per = [o.timed_steps(budget)[0] for _ in range(K)]
+    per_unit = statistics.mean(per)
+    step_s = per_unit * w.units * w.layers
+    v = w.batch / step_s
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1, "steps": K,
+        "warmup": W, "ms_per_step": step_s * 1000.0, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generator)",
+        "config": {"workload": w.name, "layers": w.layers, "batch_per_gpu": w.batch, "seq_len": w.seq_len},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": (f"each step: float64 oracle decode steps of one unit of layer 0 for about "
+                                    f"{budget:.1f} s, scaled to {w.units} units x {w.layers} layers")},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_env()
+    w = workload_from(args)
+    if args.impl == "reference":
+        line = run_reference(args, w, ws, rank)
+    else:
+        line = run_ours(args, w, ws, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,213 @@
+/*
+ * shadowkv.h — C ABI of the ShadowKV decode-step sparse attention library
+ * (libshadowkv.so, sm_103a / GB300).
+ *
+ * The method: "ShadowKV: KV Cache in Shadows for High-Throughput Long-Context
+ * LLM Inference".  The calls map one to one onto the two algorithms of the
+ * Chinese digest of that paper (section A2): Algorithm 1 (pre-filling) is
+ * shadowkv_prefill_index, Algorithm 2 (decoding) is shadowkv_decode_step.
+ * The analytical models (equivalent bandwidth, memory savings, compression
+ * ratio) are those of the English summary, section 3.4 and the appendix A.2
+ * memory-savings formula.
+ *
+ * Conventions for every call:
+ *  - All tensors are dense row-major in the storage dtype of the config
+ *    (float32 or bfloat16), 16-byte aligned.  "dev" marks device memory of the
+ *    current CUDA device; "host" marks page-locked host memory.
+ *  - Nothing throws across this ABI.  Every int-returning call returns
+ *    SKV_OK (0) or one of the negative SKV_ERR_* codes below.
+ *  - Calls that take streams enqueue work and return; they do not
+ *    synchronise unless stated.  A handle must not be used from two host
+ *    threads at once.
+ *  - Kernels that index with chunk ids, slots or positions range-check them;
+ *    a failed check sets a device error word and skips the access.  The word
+ *    is read (with a synchronisation) by shadowkv_stats, which then returns
+ *    SKV_ERR_DEVICE_BOUNDS or SKV_ERR_TIMEOUT.
+ */
+#ifndef SHADOWKV_H
+#define SHADOWKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Error codes. */
+#define SKV_OK                 0
+#define SKV_ERR_INVALID       -1  /* bad config, null or misaligned pointer, bad handle */
+#define SKV_ERR_OOM           -2  /* device allocation failed (all partial state freed) */
+#define SKV_ERR_NOT_PINNED    -3  /* v_place = host but V is not page-locked host memory */
+#define SKV_ERR_CUDA          -4  /* a CUDA runtime/driver call failed */
+#define SKV_ERR_DEVICE_BOUNDS -5  /* a kernel met an out-of-range index (access skipped) */
+#define SKV_ERR_TIMEOUT       -6  /* a kernel's bounded wait ran out (work abandoned) */
+#define SKV_ERR_STEP_LIMIT    -7  /* more decode steps than max_new_tokens */
+#define SKV_ERR_UNSUPPORTED   -8  /* valid for the method, not built for this device/shape */
+
+/* A CUDA stream (cudaStream_t) without pulling in the CUDA headers. */
+typedef struct CUstream_st* skv_stream;
+
+typedef enum { SKV_F32 = 0, SKV_BF16 = 1 } skv_dtype;
+typedef enum { SKV_V_HBM = 0, SKV_V_HOST = 1 } skv_vplace;
+
+/*
+ * Sizes of one layer.  Notation of the pages: b batch, H KV heads, G = n_q/H
+ * query heads per KV head, d head dim, r rank, C chunk, K selected chunks,
+ * O outlier chunks, W local-window tokens, S context length.
+ * Requirements: d = 128, C = 8, G in {1, 2, 4, 8}, n_q = G*H, S % C == 0,
+ * W % C == 0, n_c = S/C - O - W/C >= K >= 1, O >= 0, 8 <= r <= 256 and
+ * r % 8 == 0, max_new_tokens >= 1.
+ */
+typedef struct {
+    int32_t batch;          /* b */
+    int32_t n_kv_heads;     /* H */
+    int32_t n_q_heads;      /* H*G */
+    int32_t head_dim;       /* d */
+    int32_t rank;           /* r, A is shared by the H heads of one batch element */
+    int32_t chunk;          /* C */
+    int32_t n_select;       /* K chunks selected per KV head and step */
+    int32_t n_outlier;      /* O static outlier chunks per KV head */
+    int32_t local_window;   /* W prefill tokens kept exact (plus every decode token) */
+    int32_t max_new_tokens; /* decode steps the handle accepts */
+    int64_t seq_len;        /* S */
+    double  rope_base;      /* theta_i = rope_base^(-2i/d), half-split pairs (i, i+d/2) */
+    int32_t dtype;          /* skv_dtype: storage of A, B, V, q, keys, landmarks, out */
+    int32_t v_place;        /* skv_vplace of V */
+} skv_config;
+
+typedef struct skv_layer skv_layer;   /* opaque; one per layer */
+
+/* Host-only check of a config against the requirements above.  No CUDA call. */
+int shadowkv_validate_config(const skv_config* cfg);
+
+/*
+ * Algorithm 1 (pre-filling) for one layer: rebuilds K~ = RoPE(A.B) for every
+ * context token, takes chunk means as landmarks, picks per (b, h) the O
+ * chunks outside the local window with the lowest minimum cosine between a
+ * token key and its chunk mean (lower chunk id first on ties), removes them
+ * from the landmarks, and gathers the outlier chunks' K~/V and the local
+ * window's K~/V to the GPU.
+ *
+ *   A  dev  [b][S][r]      low-rank token coordinates (borrowed)
+ *   B  dev  [b][H][r][d]   per-head bases (borrowed)
+ *   V  dev or host [b][H][S][d]  values; host memory must be page-locked
+ *      (cudaHostAlloc / cudaHostRegister) when v_place = SKV_V_HOST (borrowed)
+ *
+ * A, B and V must stay valid until shadowkv_destroy: decode steps read A/B
+ * rows and V rows of the chunks they miss.  The library owns everything else.
+ * Runs on `stream` and synchronises it before returning.  On error *out is
+ * NULL and nothing is leaked.
+ */
+int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, const void* V,
+                           skv_stream stream, skv_layer** out);
+
+/*
+ * Algorithm 2 (decoding), one step of one layer:
+ *   1. appends (k_new, v_new) to the exact local set;
+ *   2. P = q.L^T for the G query heads of every KV head (q-head j belongs to
+ *      KV head j / G); S2 = max over the group of softmax(P / sqrt(d)) over the
+ *      n_c selectable chunks; I = ArgTopK(S2, K), lower chunk id first on ties;
+ *   3. index scan against the previous step's I: hit chunks keep their cache
+ *      slot, missed chunks take the freed slots;
+ *   4. rebuilds the missed chunks' keys RoPE(A[rows].B[b][h]) into their slots
+ *      (main stream) while their values are gathered from V (side stream);
+ *   5. out = softmax(q.K^T / sqrt(d)).V over the O*C outlier tokens, the K*C
+ *      cached tokens and the W + t + 1 local tokens (t = 0-based step).
+ *
+ *   q      dev [b][H*G][d]  post-RoPE queries at position S + t
+ *   k_new  dev [b][H][d]    post-RoPE key of the new token
+ *   v_new  dev [b][H][d]
+ *   out    dev [b][H*G][d]  written
+ *   sel_out dev int32 [b][H][K] or NULL: I as original chunk ids, ascending
+ *   main, side: streams; side may be NULL or equal to main (then all work runs
+ *   on main).  The library orders the two with its own events; the step is
+ *   complete when `main` reaches the end of the enqueued work.
+ */
+int shadowkv_decode_step(skv_layer* layer, const void* q, const void* k_new, const void* v_new,
+                         void* out, int32_t* sel_out, skv_stream main, skv_stream side);
+
+/* Phases timed when profiling is on (CUDA events on the launching stream). */
+#define SKV_PH_SCORE   0
+#define SKV_PH_SELECT  1
+#define SKV_PH_REBUILD 2
+#define SKV_PH_FETCH   3
+#define SKV_PH_ATTN    4
+#define SKV_NPHASE     5
+
+typedef struct {
+    int64_t steps;              /* decode steps taken */
+    int64_t units;              /* b*H */
+    int64_t n_select;           /* K */
+    int64_t hits, misses;       /* summed over steps and units */
+    double  alpha_last;         /* hit rate of the last step */
+    double  alpha_mean;         /* mean hit rate over steps t >= 1 (0 if none) */
+    double  hbm_bytes;          /* algorithmic HBM bytes, summed over steps */
+    double  link_bytes;         /* algorithmic host-link bytes (v_place = host) */
+    double  scratch_bytes;      /* implementation scratch traffic (logits, partials) */
+    double  phase_ms[SKV_NPHASE];        /* summed event time per phase (profiling) */
+    int64_t phase_launches[SKV_NPHASE];  /* launches timed per phase */
+    int32_t device_error;       /* 0, SKV_ERR_DEVICE_BOUNDS or SKV_ERR_TIMEOUT */
+} skv_stats;
+
+/*
+ * Synchronises the layer's streams, reads the device counters and the error
+ * word, and fills *out.  Returns the device error (if any) after filling *out.
+ */
+int shadowkv_stats(skv_layer* layer, skv_stats* out);
+int shadowkv_reset_stats(skv_layer* layer);
+
+/* Per-phase CUDA-event timing on (1) or off (0, the default). */
+int shadowkv_set_profiling(skv_layer* layer, int enable);
+
+/*
+ * Inspection: copies one internal buffer (device to device, on `stream`) into
+ * caller memory `dst` of at least shadowkv_export_size(layer, field) bytes.
+ */
+#define SKV_F_LANDMARKS     0   /* [b*H][n_c][d] dtype, compacted (outliers removed) */
+#define SKV_F_CHUNK_IDS     1   /* [b*H][n_c] int32: original chunk id of each landmark */
+#define SKV_F_OUTLIER_IDS   2   /* [b*H][O] int32, ascending */
+#define SKV_F_MIN_COS       3   /* [b*H][S/C - W/C] float32 */
+#define SKV_F_K_OUTLIER     4   /* [b*H][O*C][d] dtype */
+#define SKV_F_V_OUTLIER     5   /* [b*H][O*C][d] dtype */
+#define SKV_F_K_LOCAL       6   /* [b*H][W + max_new_tokens][d] dtype */
+#define SKV_F_V_LOCAL       7   /* [b*H][W + max_new_tokens][d] dtype */
+#define SKV_F_K_CACHE       8   /* [b*H][K][C][d] dtype, by slot */
+#define SKV_F_V_CACHE       9   /* [b*H][K][C][d] dtype, by slot */
+#define SKV_F_SELECTION    10   /* [b*H][K] int32: current I, ascending chunk ids */
+#define SKV_F_SLOT_OF_SEL  11   /* [b*H][K] int32: cache slot of each entry of I */
+#define SKV_F_MISS_COUNT   12   /* [b*H] int32: misses of the last step */
+#define SKV_F_HITS_PER_STEP 13  /* [max_new_tokens] int32: hits summed over units */
+#define SKV_NFIELD         14
+int64_t shadowkv_export_size(const skv_layer* layer, int field);
+int shadowkv_export(skv_layer* layer, int field, void* dst, size_t bytes, skv_stream stream);
+
+/*
+ * Analytical models of the pages, host only:
+ *   eq_bandwidth_gbs = 2 S B_GPU / (S/C + 2(K+O)C + (1-alpha) K C B_GPU / B_link)
+ *   memory_savings   = 2SM / (SM/C + 2(K+O)C + Sr + rM), literal, M = H d (the
+ *                      key width of one token across the KV heads, in elements)
+ *   compression      = S d' / (r (S + d')), d' = H d (A is shared by the heads)
+ * plus the algorithmic bytes of one decode step of one layer at hit rate alpha
+ * and step t, and the predicted step time of that layer
+ *   t_pred = hbm_bytes / B_GPU + link_bytes / B_link.
+ */
+typedef struct {
+    double eq_bandwidth_gbs;
+    double memory_savings;
+    double compression_ratio;
+    double hbm_bytes_per_step;
+    double link_bytes_per_step;
+    double t_pred_us;
+} skv_model;
+int shadowkv_model(const skv_config* cfg, double alpha, int64_t t, double b_gpu_gbs,
+                   double b_link_gbs, skv_model* out);
+
+void shadowkv_destroy(skv_layer* layer);   /* frees everything the handle owns; NULL ok */
+const char* shadowkv_strerror(int code);
+int shadowkv_version(void);                 /* major*10000 + minor*100 + patch */
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SHADOWKV_H */

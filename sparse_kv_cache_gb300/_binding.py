@@ -1,0 +1,205 @@
+"""ctypes binding of libshadowkv.so (argument marshalling only).
+
+Every step of the decode path runs in the library's CUDA kernels; this module
+only turns torch tensors into pointers and streams into handles, and checks
+return codes.  There is no fallback: if the library is missing, loading fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libshadowkv.so")
+
+SKV_F32, SKV_BF16 = 0, 1
+SKV_V_HBM, SKV_V_HOST = 0, 1
+PHASES = ("score", "select", "rebuild", "fetch", "attn")
+FIELDS = {
+    "landmarks": 0, "chunk_ids": 1, "outlier_ids": 2, "min_cos": 3, "k_outlier": 4, "v_outlier": 5,
+    "k_local": 6, "v_local": 7, "k_cache": 8, "v_cache": 9, "selection": 10, "slot_of_sel": 11,
+    "miss_count": 12, "hits_per_step": 13,
+}
+ERRORS = {0: "OK", -1: "INVALID", -2: "OOM", -3: "NOT_PINNED", -4: "CUDA", -5: "DEVICE_BOUNDS",
+          -6: "TIMEOUT", -7: "STEP_LIMIT", -8: "UNSUPPORTED"}
+EXPORTED = ("shadowkv_validate_config", "shadowkv_prefill_index", "shadowkv_decode_step",
+            "shadowkv_stats", "shadowkv_reset_stats", "shadowkv_set_profiling",
+            "shadowkv_export_size", "shadowkv_export", "shadowkv_model", "shadowkv_destroy",
+            "shadowkv_strerror", "shadowkv_version")
+
+
+class SkvConfig(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("n_q_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("rank", ctypes.c_int32), ("chunk", ctypes.c_int32),
+                ("n_select", ctypes.c_int32), ("n_outlier", ctypes.c_int32),
+                ("local_window", ctypes.c_int32), ("max_new_tokens", ctypes.c_int32),
+                ("seq_len", ctypes.c_int64), ("rope_base", ctypes.c_double),
+                ("dtype", ctypes.c_int32), ("v_place", ctypes.c_int32)]
+
+
+class SkvStats(ctypes.Structure):
+    _fields_ = [("steps", ctypes.c_int64), ("units", ctypes.c_int64), ("n_select", ctypes.c_int64),
+                ("hits", ctypes.c_int64), ("misses", ctypes.c_int64),
+                ("alpha_last", ctypes.c_double), ("alpha_mean", ctypes.c_double),
+                ("hbm_bytes", ctypes.c_double), ("link_bytes", ctypes.c_double),
+                ("scratch_bytes", ctypes.c_double),
+                ("phase_ms", ctypes.c_double * 5), ("phase_launches", ctypes.c_int64 * 5),
+                ("device_error", ctypes.c_int32)]
+
+
+class SkvModel(ctypes.Structure):
+    _fields_ = [("eq_bandwidth_gbs", ctypes.c_double), ("memory_savings", ctypes.c_double),
+                ("compression_ratio", ctypes.c_double), ("hbm_bytes_per_step", ctypes.c_double),
+                ("link_bytes_per_step", ctypes.c_double), ("t_pred_us", ctypes.c_double)]
+
+
+class ShadowKVError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {ERRORS.get(code, code)} ({strerror(code)})")
+
+
+_lib = None
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libshadowkv.so (built in-tree by ``sparse_kv_cache_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise ImportError(f"{p} is missing: build it with sparse_kv_cache_gb300.build.build()")
+    lib = ctypes.CDLL(p)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    lib.shadowkv_validate_config.argtypes = [ctypes.POINTER(SkvConfig)]
+    lib.shadowkv_prefill_index.argtypes = [ctypes.POINTER(SkvConfig), vp, vp, vp, vp, ctypes.POINTER(vp)]
+    lib.shadowkv_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.shadowkv_stats.argtypes = [vp, ctypes.POINTER(SkvStats)]
+    lib.shadowkv_reset_stats.argtypes = [vp]
+    lib.shadowkv_set_profiling.argtypes = [vp, i32]
+    lib.shadowkv_export_size.argtypes = [vp, i32]
+    lib.shadowkv_export_size.restype = i64
+    lib.shadowkv_export.argtypes = [vp, i32, vp, sz, vp]
+    lib.shadowkv_model.argtypes = [ctypes.POINTER(SkvConfig), ctypes.c_double, i64, ctypes.c_double,
+                                   ctypes.c_double, ctypes.POINTER(SkvModel)]
+    lib.shadowkv_destroy.argtypes = [vp]
+    lib.shadowkv_destroy.restype = None
+    lib.shadowkv_strerror.argtypes = [i32]
+    lib.shadowkv_strerror.restype = ctypes.c_char_p
+    lib.shadowkv_version.argtypes = []
+    for name in ("shadowkv_validate_config", "shadowkv_prefill_index", "shadowkv_decode_step",
+                 "shadowkv_stats", "shadowkv_reset_stats", "shadowkv_set_profiling",
+                 "shadowkv_export", "shadowkv_model", "shadowkv_version"):
+        getattr(lib, name).restype = i32
+    _lib = lib
+    return lib
+
+
+def strerror(code: int) -> str:
+    return load().shadowkv_strerror(code).decode()
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise ShadowKVError(code, where)
+
+
+def make_config(w=None, **kw) -> SkvConfig:
+    """Config from a ``workload.Workload`` (or keyword fields)."""
+    f = {}
+    if w is not None:
+        f = dict(batch=w.batch, n_kv_heads=w.n_kv_heads, n_q_heads=w.n_q_heads,
+                 head_dim=w.head_dim, rank=w.rank, chunk=w.chunk, n_select=w.n_select,
+                 n_outlier=w.n_outlier, local_window=w.local_window, max_new_tokens=w.steps,
+                 seq_len=w.seq_len, rope_base=w.rope_base,
+                 dtype=SKV_BF16 if w.dtype == "bf16" else SKV_F32,
+                 v_place=SKV_V_HOST if w.v_place == "host" else SKV_V_HBM)
+    f.update(kw)
+    return SkvConfig(**f)
+
+
+def validate_config(cfg: SkvConfig) -> int:
+    return load().shadowkv_validate_config(ctypes.byref(cfg))
+
+
+def model(cfg: SkvConfig, alpha: float, t: int, b_gpu_gbs: float, b_link_gbs: float) -> dict:
+    out = SkvModel()
+    _check(load().shadowkv_model(ctypes.byref(cfg), alpha, t, b_gpu_gbs, b_link_gbs, ctypes.byref(out)),
+           "shadowkv_model")
+    return {k: getattr(out, k) for k, _ in SkvModel._fields_}
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return s.cuda_stream if hasattr(s, "cuda_stream") else int(s)
+
+
+class Layer:
+    """One layer's ShadowKV state (the handle of shadowkv_prefill_index)."""
+
+    def __init__(self, cfg: SkvConfig, A, B, V, stream=None):
+        lib = load()
+        self.cfg = cfg
+        self._keep = (A, B, V)   # the library borrows these
+        h = ctypes.c_void_p()
+        _check(lib.shadowkv_prefill_index(ctypes.byref(cfg), _ptr(A), _ptr(B), _ptr(V), _stream(stream),
+                                          ctypes.byref(h)), "shadowkv_prefill_index")
+        self._h = h
+
+    @property
+    def handle(self) -> int:
+        return self._h.value
+
+    def decode_step(self, q, k_new, v_new, out, sel_out=None, main=None, side=None):
+        _check(load().shadowkv_decode_step(self._h, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out),
+                                           _ptr(sel_out), _stream(main),
+                                           None if side is None else _stream(side)),
+               "shadowkv_decode_step")
+
+    def decode_step_raw(self, q, k_new, v_new, out, sel_out, main, side) -> int:
+        """Same call with integer pointers/handles; returns the status code."""
+        return load().shadowkv_decode_step(self._h, q, k_new, v_new, out, sel_out, main, side)
+
+    def stats(self, check: bool = True) -> dict:
+        s = SkvStats()
+        rc = load().shadowkv_stats(self._h, ctypes.byref(s))
+        if check:
+            _check(rc, "shadowkv_stats")
+        d = {k: getattr(s, k) for k, _ in SkvStats._fields_ if k not in ("phase_ms", "phase_launches")}
+        d["phase_ms"] = dict(zip(PHASES, list(s.phase_ms)))
+        d["phase_launches"] = dict(zip(PHASES, list(s.phase_launches)))
+        d["status"] = rc
+        return d
+
+    def reset_stats(self):
+        _check(load().shadowkv_reset_stats(self._h), "shadowkv_reset_stats")
+
+    def set_profiling(self, on: bool):
+        _check(load().shadowkv_set_profiling(self._h, 1 if on else 0), "shadowkv_set_profiling")
+
+    def export_size(self, field: str) -> int:
+        return load().shadowkv_export_size(self._h, FIELDS[field])
+
+    def export(self, field: str, dst, stream=None):
+        _check(load().shadowkv_export(self._h, FIELDS[field], _ptr(dst),
+                                      dst.numel() * dst.element_size(), _stream(stream)),
+               f"shadowkv_export({field})")
+
+    def close(self):
+        if getattr(self, "_h", None) and self._h.value:
+            load().shadowkv_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

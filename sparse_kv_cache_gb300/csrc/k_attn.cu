@@ -1,0 +1,208 @@
+// Exact sparse attention over the assembled key/value set.
+//
+// ShadowKV (English summary, section 3.4, "Assembly of the final sparse KV
+// cache": K = [K_outlier; RoPE(K_sparse); K_new], V likewise, then exact
+// attention; Chinese digest section A2, Algorithm 2, and A7 "implementation
+// details": attention itself was a library flash kernel on the A100).
+//
+// Split-K flash-decode.  Per (unit, split) one CTA takes 256 consecutive
+// tokens of the virtual sequence [outliers | cache slots | local] and all G
+// query heads of the unit: scores by half-warp dot products with a
+// transpose-reduction, a block max and exp, then p.V with each half-warp
+// owning 16 tokens and every lane 8 dims, reduced across half-warps in shared
+// memory.  It writes (max, sum, acc[d]) per head; the CTA that finishes last
+// for its unit (atomic ticket after a memory fence) merges the partials in
+// fp32 and writes the output row.  Each key and value byte is read once.
+#include <math_constants.h>
+
+#include "skv_common.cuh"
+#include "skv_internal.h"
+
+namespace skv {
+
+constexpr int kPartPitch = kD + 4;   // acc[d], max, sum, pad
+
+template <typename T>
+__device__ __forceinline__ const T* row_ptr(const AttnParams& p, const void* out_b, const void* c_b,
+                                            const void* loc_b, int u, int tau) {
+    if (tau < p.n_out) return static_cast<const T*>(out_b) + (static_cast<int64_t>(u) * p.n_out + tau) * kD;
+    tau -= p.n_out;
+    if (tau < p.n_cache) return static_cast<const T*>(c_b) + (static_cast<int64_t>(u) * p.n_cache + tau) * kD;
+    tau -= p.n_cache;
+    return static_cast<const T*>(loc_b) + (static_cast<int64_t>(u) * p.loc_cap + tau) * kD;
+}
+
+template <typename T, int G>
+__global__ void __launch_bounds__(256) k_attn(AttnParams p) {
+    extern __shared__ __align__(16) float sm[];
+    float* sS = sm;                          // [256][G] scores, then probabilities
+    float* sRed = sm + kAttnSeg * G;         // [16][G][d]
+    __shared__ float red_m[8][G], red_l[8][G];
+    __shared__ int s_last;
+
+    const int u = blockIdx.y, split = blockIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, hl = lane & 15, half = lane >> 4;
+    const int ntot = p.n_out + p.n_cache + p.n_loc;
+    const int seg0 = split * kAttnSeg;
+
+    float qv[G][8];
+#pragma unroll
+    for (int g = 0; g < G; ++g) load8(static_cast<const T*>(p.q) + (static_cast<int64_t>(u) * G + g) * kD + hl * 8, qv[g]);
+
+    // ---- scores
+#pragma unroll
+    for (int round = 0; round < 2; ++round) {
+        const int tb = warp * 32 + round * 16 + half * 8;
+        float acc[G][8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const int tau = seg0 + tb + c;
+            float v[8];
+            if (tau < ntot) {
+                load8(row_ptr<T>(p, p.k_out, p.k_c, p.k_loc, u, tau) + hl * 8, v);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) v[k] = 0.f;
+            }
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float a = 0.f;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) a = fmaf(qv[g][k], v[k], a);
+                acc[g][c] = a;
+            }
+        }
+        float s[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) s[g] = transpose_reduce8(acc[g], hl) * p.scale;
+        const int tl = tb + (hl >> 1);
+        if ((hl & 1) == 0) {
+            const bool valid = seg0 + tl < ntot;
+#pragma unroll
+            for (int g = 0; g < G; ++g) sS[tl * G + g] = valid ? s[g] : -CUDART_INF_F;
+        }
+    }
+    __syncthreads();
+
+    // ---- max and exp per head over the 256 tokens
+    float M[G], Lsum[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const float x = warp_max(sS[tid * G + g]);
+        if (lane == 0) red_m[warp][g] = x;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        float x = red_m[0][g];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) x = fmaxf(x, red_m[w][g]);
+        M[g] = x;
+        const float sv = sS[tid * G + g];
+        const float pv = (sv == -CUDART_INF_F) ? 0.f : __expf(sv - x);
+        sS[tid * G + g] = pv;
+        const float ws = warp_sum(pv);
+        if (lane == 0) red_l[warp][g] = ws;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        float x = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) x += red_l[w][g];
+        Lsum[g] = x;
+    }
+
+    // ---- p . V
+    const int hw = warp * 2 + half;
+    float acc[G][8];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[g][k] = 0.f;
+#pragma unroll 4
+    for (int tl = hw; tl < kAttnSeg; tl += 16) {
+        const int tau = seg0 + tl;
+        if (tau >= ntot) break;
+        float v[8];
+        load8(row_ptr<T>(p, p.v_out, p.v_c, p.v_loc, u, tau) + hl * 8, v);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const float pg = sS[tl * G + g];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc[g][k] = fmaf(pg, v[k], acc[g][k]);
+        }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        float* r = sRed + (hw * G + g) * kD + hl * 8;
+        reinterpret_cast<float4*>(r)[0] = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
+        reinterpret_cast<float4*>(r)[1] = make_float4(acc[g][4], acc[g][5], acc[g][6], acc[g][7]);
+    }
+    __syncthreads();
+    float* mypart = p.part + (static_cast<int64_t>(u) * p.nsplit + split) * G * kPartPitch;
+    for (int o = tid; o < G * kD; o += 256) {
+        float x = 0.f;
+#pragma unroll
+        for (int h = 0; h < 16; ++h) x += sRed[h * G * kD + o];
+        const int g = o / kD, dim = o % kD;
+        mypart[g * kPartPitch + dim] = x;
+        if (dim == 0) {
+            mypart[g * kPartPitch + kD] = M[g];
+            mypart[g * kPartPitch + kD + 1] = Lsum[g];
+        }
+    }
+
+    // ---- the last CTA of this unit merges the partials
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = (atomicAdd(p.counter + u, 1) == p.nsplit - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const float* parts = p.part + static_cast<int64_t>(u) * p.nsplit * G * kPartPitch;
+    for (int o = tid; o < G * kD; o += 256) {
+        const int g = o / kD, dim = o % kD;
+        float mx = -CUDART_INF_F;
+        for (int s = 0; s < p.nsplit; ++s) mx = fmaxf(mx, __ldcg(parts + (s * G + g) * kPartPitch + kD));
+        float ls = 0.f, a = 0.f;
+        for (int s = 0; s < p.nsplit; ++s) {
+            const float* ps = parts + (s * G + g) * kPartPitch;
+            const float m = __ldcg(ps + kD);
+            const float w = (m == -CUDART_INF_F) ? 0.f : __expf(m - mx);
+            ls = fmaf(__ldcg(ps + kD + 1), w, ls);
+            a = fmaf(__ldcg(ps + dim), w, a);
+        }
+        static_cast<T*>(p.out)[(static_cast<int64_t>(u) * G + g) * kD + dim] = from_f<T>(a / ls);
+    }
+    if (tid == 0) p.counter[u] = 0;
+}
+
+template <typename T, int G>
+static int launch_t(const AttnParams& p, cudaStream_t s) {
+    const size_t smem = (static_cast<size_t>(kAttnSeg) * G + 16 * G * kD) * 4;
+    cudaFuncSetAttribute(k_attn<T, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    k_attn<T, G><<<dim3(p.nsplit, p.U), 256, smem, s>>>(p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_attn(int dtype, const AttnParams& p, cudaStream_t s) {
+    if (dtype == 1) {
+        switch (p.G) {
+            case 1: return launch_t<__nv_bfloat16, 1>(p, s);
+            case 2: return launch_t<__nv_bfloat16, 2>(p, s);
+            case 4: return launch_t<__nv_bfloat16, 4>(p, s);
+            case 8: return launch_t<__nv_bfloat16, 8>(p, s);
+        }
+    } else {
+        switch (p.G) {
+            case 1: return launch_t<float, 1>(p, s);
+            case 2: return launch_t<float, 2>(p, s);
+            case 4: return launch_t<float, 4>(p, s);
+            case 8: return launch_t<float, 8>(p, s);
+        }
+    }
+    return -1;
+}
+
+}  // namespace skv

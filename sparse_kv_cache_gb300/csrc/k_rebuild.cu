@@ -1,0 +1,338 @@
+// Sparse key reconstruction: K~ = RoPE(Gather(A, chunks) . B_h).
+//
+// ShadowKV (English summary, section 3.4, "Sparse KV Reconstruction and
+// Overlapping Strategy": K_sparse = MatMul(Gather(A, I_miss), B), then RoPE at
+// the tokens' own positions; Chinese digest section A2, Algorithm 2).  The
+// same kernels serve Algorithm 1's pre-filling in "statistics" mode: instead
+// of storing the keys they emit each chunk's mean (the landmark, summary
+// section 3.4 "Landmark Construction") and the minimum cosine between a token
+// key and that mean (Algorithm 1: CosineSimilarity, Min).
+//
+// A tile is 16 chunks = 128 token rows of one (batch, KV head) unit.
+//  * bf16: a tcgen05 tile.  The producer lane loads the unit's B slice
+//    (stored transposed, [d][r], K-major) and the 16 chunks' A rows (8 rows
+//    each, from anywhere in A) with 2-D TMA copies in 64-column (128-byte,
+//    swizzled) blocks; zero fill covers columns past r.  One elected thread
+//    issues M=128, N=128, K=16 bf16 MMAs with an fp32 accumulator in tensor
+//    memory; the four warps read their 32 rows back with tcgen05.ld.
+//  * fp32: CUDA-core FMAs, one thread per row, B broadcast from shared memory
+//    (tf32 tensor cores would not meet fp32 accuracy).
+// Epilogue (both): RoPE with angles composed from two tables,
+// cos/sin(pos*theta) = product of the (pos & 255) and (pos >> 8)*256 entries,
+// built on the host in double precision; then either the bf16/fp32 key rows
+// go to their destination slot, or the statistics are formed in fp32.
+#include <math_constants.h>
+
+#include "skv_common.cuh"
+#include "skv_internal.h"
+
+namespace skv {
+
+constexpr int kRows = kTileChunks * kC;   // 128
+constexpr int kStagePitch = kD + 4;       // fp32 staging row pitch (floats)
+
+struct TileInfo {
+    int chunk;   // original chunk id, -1 if the row is not valid
+    int dst;     // destination chunk slot
+};
+
+__device__ __forceinline__ void rope_pair(const RebuildParams& p, int pos, int i, float& a, float& b) {
+    const float2 lo = p.rope_lo[(pos & 255) * (kD / 2) + i];
+    const float2 hi = p.rope_hi[(pos >> 8) * (kD / 2) + i];
+    const float c = hi.x * lo.x - hi.y * lo.y;
+    const float s = hi.y * lo.x + hi.x * lo.y;
+    const float x = a, y = b;
+    a = x * c - y * s;
+    b = x * s + y * c;
+}
+
+// Rotate one row half (dims [32h, 32h+32) and [64+32h, 64+32h+32)) and store it.
+template <typename OutT>
+__device__ __forceinline__ void finish_half(const RebuildParams& p, int u, int row, const TileInfo& ti, int h,
+                                            float (&v0)[32], float (&v1)[32], float* stage) {
+    const bool valid = ti.chunk >= 0;
+    const int pos = valid ? ti.chunk * kC + (row & 7) : 0;
+    if (valid) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) rope_pair(p, pos, 32 * h + i, v0[i], v1[i]);
+    }
+    if (p.mode == 0) {
+        if (!valid) return;
+        OutT* dst = static_cast<OutT*>(p.dst) + u * p.dst_us + (static_cast<int64_t>(ti.dst) * kC + (row & 7)) * kD;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float w[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) w[k] = v0[8 * q + k];
+            store8(dst + 32 * h + 8 * q, w);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) w[k] = v1[8 * q + k];
+            store8(dst + kD / 2 + 32 * h + 8 * q, w);
+        }
+    } else {
+        float* srow = stage + row * kStagePitch;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            srow[32 * h + i] = v0[i];
+            srow[kD / 2 + 32 * h + i] = v1[i];
+        }
+    }
+}
+
+// Landmarks and min-cos of the tile's chunks from the fp32 staging tile
+// (needs all 128 threads; `smean` holds 16 x d floats).
+__device__ void tile_stats(const RebuildParams& p, int u, const TileInfo* ti, const float* stage, float* smean) {
+    const int tid = threadIdx.x;
+    {
+        const int c = tid >> 3, d0 = (tid & 7) * 16;
+        const float* base = stage + c * kC * kStagePitch;
+        float acc[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+#pragma unroll
+        for (int t = 0; t < kC; ++t)
+#pragma unroll
+            for (int k = 0; k < 16; ++k) acc[k] += base[t * kStagePitch + d0 + k];
+        float* lf = ti[c].chunk >= 0 ? p.Lfull + (u * p.stats_us + ti[c].chunk) * kD + d0 : nullptr;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const float mval = acc[k] * (1.0f / kC);
+            smean[c * kD + d0 + k] = mval;
+            if (lf) lf[k] = mval;
+        }
+    }
+    __syncthreads();
+    const int row = tid, c = row >> 3;
+    const float* x = stage + row * kStagePitch;
+    const float* m = smean + c * kD;
+    float dot = 0.f, nx = 0.f, nm = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < kD; ++k) {
+        const float a = x[k], b = m[k];
+        dot = fmaf(a, b, dot);
+        nx = fmaf(a, a, nx);
+        nm = fmaf(b, b, nm);
+    }
+    float cosv = dot / fmaxf(sqrtf(nx) * sqrtf(nm), 1e-12f);
+#pragma unroll
+    for (int o = 1; o < kC; o <<= 1) cosv = fminf(cosv, __shfl_xor_sync(0xffffffffu, cosv, o));
+    if ((row & 7) == 0 && ti[c].chunk >= 0) p.mcos[u * p.stats_us + ti[c].chunk] = cosv;
+}
+
+// Resolve the tile's chunk ids and destination slots; returns the number of
+// chunks in this tile, or 0 if the CTA has nothing to do.
+__device__ int load_tile_info(const RebuildParams& p, int u, int tile, TileInfo* ti) {
+    int count = p.cnt ? p.cnt[u] : p.count_const;
+    if (count < 0 || count > p.list_cap) {
+        if (threadIdx.x == 0) set_err(p.err, DEV_ERR_BOUNDS, 401);
+        count = 0;
+    }
+    const int first = tile * kTileChunks;
+    if (first >= count) return 0;
+    const int nch = min(kTileChunks, count - first);
+    if (threadIdx.x < kTileChunks) {
+        const int c = threadIdx.x;
+        TileInfo t{-1, 0};
+        if (c < nch) {
+            const int idx = first + c;
+            const int ch = p.list ? p.list[u * p.list_us + idx] : p.list_base + idx;
+            const int dst = p.dst_idx ? p.dst_idx[u * p.list_us + idx] : idx;
+            if (ch < 0 || ch >= p.nchunk || (p.mode == 0 && (dst < 0 || dst >= p.dst_cap)) ||
+                (p.mode == 1 && ch >= p.stats_us)) {
+                set_err(p.err, DEV_ERR_BOUNDS, 402);
+            } else {
+                t.chunk = ch;
+                t.dst = dst;
+            }
+        }
+        ti[c] = t;
+    }
+    return nch;
+}
+
+// ------------------------------------------------------------------ tcgen05 path
+template <typename OutT>
+__global__ void __launch_bounds__(128, 1) k_rebuild_tc(const __grid_constant__ CUtensorMap tmA,
+                                                        const __grid_constant__ CUtensorMap tmB, RebuildParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ uint64_t bar_tma, bar_mma;
+    __shared__ uint32_t tmem_slot;
+    __shared__ TileInfo ti[kTileChunks];
+    __shared__ int s_fail;
+
+    const int u = blockIdx.y, tile = blockIdx.x, tid = threadIdx.x, warp = tid >> 5;
+    const int nch = load_tile_info(p, u, tile, ti);
+    if (nch == 0) return;   // uniform: every thread computed the same count
+    const int nkb = p.nkb;
+    uint8_t* sA = smem;                      // nkb x [128 rows][128 B]
+    uint8_t* sB = smem + nkb * 16384;        // nkb x [128 rows][128 B]
+    if (tid == 0) {
+        mbar_init(&bar_tma, 1);
+        mbar_init(&bar_mma, 1);
+        s_fail = 0;
+        fence_mbar_init();
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_slot, 128);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    const int b = u / p.H;
+
+    if (tid == 0) {
+        int nvalid = 0;
+        for (int c = 0; c < nch; ++c) nvalid += ti[c].chunk >= 0;
+        mbar_arrive_expect_tx(&bar_tma, static_cast<uint32_t>(nkb * (16384 + nvalid * 1024)));
+        for (int kb = 0; kb < nkb; ++kb) {
+            tma_load_2d(sB + kb * 16384, &tmB, kb * 64, u * kD, &bar_tma);
+            for (int c = 0; c < nch; ++c)
+                if (ti[c].chunk >= 0)
+                    tma_load_2d(sA + kb * 16384 + c * 1024, &tmA, kb * 64,
+                                static_cast<int>(b * p.S + static_cast<int64_t>(ti[c].chunk) * kC), &bar_tma);
+        }
+        if (!mbar_wait(&bar_tma, 0)) {
+            set_err(p.err, DEV_ERR_TIMEOUT, 411);
+            (void)mbar_wait(&bar_tma, 0);
+            s_fail = 1;
+        } else {
+            tc_fence_after();
+            constexpr uint32_t idesc = idesc_bf16_f32(128, kD);
+            uint32_t acc = 0;
+            for (int kb = 0; kb < nkb; ++kb) {
+                const int ksteps = min(4, (p.r - kb * 64 + 15) / 16);
+                for (int k = 0; k < ksteps; ++k) {
+                    const uint64_t ad = smem_desc_sw128(smem_u32(sA + kb * 16384 + k * 32));
+                    const uint64_t bd = smem_desc_sw128(smem_u32(sB + kb * 16384 + k * 32));
+                    tc_mma_bf16(tmem, ad, bd, idesc, acc);
+                    acc = 1;
+                }
+            }
+            tc_commit(&bar_mma);
+        }
+    }
+    __syncthreads();
+    bool ok = !s_fail;
+    if (ok && !mbar_wait(&bar_mma, 0)) {
+        set_err(p.err, DEV_ERR_TIMEOUT, 412);
+        (void)mbar_wait(&bar_mma, 0);
+        ok = false;
+    }
+    ok = __syncthreads_and(ok);
+    tc_fence_after();
+    float* stage = reinterpret_cast<float*>(smem);            // reused once the MMAs are done
+    float* smean = stage + kRows * kStagePitch;
+    const int row = tid;
+    const TileInfo mine = ti[row >> 3];
+    if (ok) {
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+            float v0[32], v1[32];
+            tmem_ld32(lane_base + 32 * h, v0);
+            tmem_ld32(lane_base + kD / 2 + 32 * h, v1);
+            tmem_ld_wait();
+            finish_half<OutT>(p, u, row, mine, h, v0, v1, stage);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (ok && p.mode == 1) tile_stats(p, u, ti, stage, smean);
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 128);
+    }
+}
+
+// ------------------------------------------------------------------ fp32 CUDA-core path
+__global__ void __launch_bounds__(128) k_rebuild_f32(RebuildParams p) {
+    extern __shared__ __align__(16) uint8_t smem_f[];
+    __shared__ TileInfo ti[kTileChunks];
+    const int u = blockIdx.y, tile = blockIdx.x, tid = threadIdx.x;
+    const int nch = load_tile_info(p, u, tile, ti);
+    if (nch == 0) return;
+    float* sB = reinterpret_cast<float*>(smem_f);                 // [r][d]
+    float* stage = sB + p.r * kD;                                  // [128][pitch]
+    float* smean = stage + kRows * kStagePitch;                    // [16][d]
+    const float* B = static_cast<const float*>(p.B) + static_cast<int64_t>(u) * p.r * kD;
+    for (int i = tid; i < p.r * kD / 4; i += 128)
+        reinterpret_cast<float4*>(sB)[i] = reinterpret_cast<const float4*>(B)[i];
+    __syncthreads();
+    const int row = tid;
+    const TileInfo mine = ti[row >> 3];
+    const int b = u / p.H;
+    float acc[kD];
+#pragma unroll
+    for (int k = 0; k < kD; ++k) acc[k] = 0.f;
+    if (mine.chunk >= 0) {
+        const float* arow = static_cast<const float*>(p.A) +
+                            (b * p.S + static_cast<int64_t>(mine.chunk) * kC + (row & 7)) * p.r;
+        for (int j = 0; j < p.r; ++j) {
+            const float a = arow[j];
+            const float4* brow = reinterpret_cast<const float4*>(sB + j * kD);
+#pragma unroll
+            for (int k = 0; k < kD / 4; ++k) {
+                const float4 w = brow[k];
+                acc[4 * k + 0] = fmaf(a, w.x, acc[4 * k + 0]);
+                acc[4 * k + 1] = fmaf(a, w.y, acc[4 * k + 1]);
+                acc[4 * k + 2] = fmaf(a, w.z, acc[4 * k + 2]);
+                acc[4 * k + 3] = fmaf(a, w.w, acc[4 * k + 3]);
+            }
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        float v0[32], v1[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) { v0[i] = acc[32 * h + i]; v1[i] = acc[kD / 2 + 32 * h + i]; }
+        finish_half<float>(p, u, row, mine, h, v0, v1, stage);
+    }
+    __syncthreads();
+    if (p.mode == 1) tile_stats(p, u, ti, stage, smean);
+}
+
+// ------------------------------------------------------------------ B transpose (bf16)
+// Bt[u][n][k] = B[u][k][n]: the tensor-core B operand is K-major.
+__global__ void k_transpose_B(const __nv_bfloat16* B, __nv_bfloat16* Bt, int r) {
+    const int u = blockIdx.x;
+    const __nv_bfloat16* src = B + static_cast<int64_t>(u) * r * kD;
+    __nv_bfloat16* dst = Bt + static_cast<int64_t>(u) * r * kD;
+    for (int i = threadIdx.x; i < r * kD; i += blockDim.x) {
+        const int n = i / r, k = i % r;
+        dst[i] = src[k * kD + n];
+    }
+}
+
+static size_t tc_smem(const RebuildParams& p) {
+    const size_t ops = static_cast<size_t>(p.nkb) * 2 * 16384;
+    const size_t stats = static_cast<size_t>(kRows * kStagePitch + kTileChunks * kD) * 4;
+    return (ops > stats ? ops : stats) + 1024;
+}
+
+int launch_rebuild_tc(const CUtensorMap* tmA, const CUtensorMap* tmB, const RebuildParams& p, int grid_x,
+                      cudaStream_t s) {
+    const size_t smem = tc_smem(p);
+    auto fn = k_rebuild_tc<__nv_bfloat16>;
+    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    fn<<<dim3(grid_x, p.U), 128, smem, s>>>(*tmA, *tmB, p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_rebuild_f32(const RebuildParams& p, int grid_x, cudaStream_t s) {
+    const size_t smem = (static_cast<size_t>(p.r) * kD + kRows * kStagePitch + kTileChunks * kD) * 4;
+    cudaFuncSetAttribute(k_rebuild_f32, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    k_rebuild_f32<<<dim3(grid_x, p.U), 128, smem, s>>>(p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_transpose_B(const void* B, void* Bt, int U, int r, cudaStream_t s) {
+    k_transpose_B<<<U, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(B), static_cast<__nv_bfloat16*>(Bt), r);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace skv

@@ -1,0 +1,449 @@
+// Per-KV-head top-K selection, the temporal chunk cache's index scan and the
+// append of the new token; and (prefill) the outlier choice.
+//
+// ShadowKV (Chinese digest, section A2, Algorithm 2): S = Softmax(P/sqrt(d)),
+// S1 = sum over query tokens, S2 = max_kv_group(S1), I = ArgTopK(S2, k); the
+// decoding text of the same section: an index scan finds the chunks missed
+// against the previous step and only those are rebuilt and fetched.  English
+// summary section 3.4, Steps 2-3 and "The temporal KV cache mechanism".
+// Algorithm 1: I = ArgTopK(-Min(S, dim=-1), o) picks the outliers.
+//
+// One 1024-thread CTA per (batch, KV head) unit.  Ordering by
+// S2_j = max_g exp(z_gj - lse_g) equals ordering by v_j = max_g (z_gj - lse_g)
+// (exp is increasing), so the kernel ranks v_j.  The exact K-th largest value
+// T and the last index `jlast` taken among values equal to T are found with a
+// 2048-bin histogram over [min v, max v] (monotone binning), then an exact
+// rank among the <= 256 candidates of the boundary bin (or, for a crowded bin,
+// an exact 4-pass radix select on the order-preserving integer image of the
+// floats).  The selection {v > T} U {v == T, j <= jlast} has exactly K members
+// and gives equal scores to the lower index; it is written in ascending index
+// order by a two-pass warp-segmented compaction.
+#include <math_constants.h>
+
+#include "skv_common.cuh"
+#include "skv_internal.h"
+
+namespace skv {
+
+constexpr int kBins = 2048;
+constexpr int kCand = 256;
+constexpr int kWarps = kSelThreads / 32;
+
+struct SelShared {
+    int hist[kBins];
+    float cand_v[kCand];
+    int cand_j[kCand];
+    int ncand;
+    float red_f[kWarps];
+    float red_f2[kWarps];
+    int red_i[kWarps];
+    int wpre[kWarps + 1];
+    float lse[8];
+    float vmin, vmax, T;
+    int jlast, bstar, above, total;
+};
+
+__device__ __forceinline__ uint32_t ord_key(float x) {
+    uint32_t b = __float_as_uint(x);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+__device__ __forceinline__ int bin_of(float x, float vmin, float invw) {
+    int b = static_cast<int>((x - vmin) * invw);
+    return b < 0 ? 0 : (b >= kBins ? kBins - 1 : b);
+}
+
+// Block-wide exclusive prefix sum of one int per thread; *total gets the sum.
+__device__ int block_exscan(int v, SelShared& sh, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sh.red_i[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = sh.red_i[lane];
+        int s = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        sh.wpre[lane] = s - w;
+        if (lane == 31) sh.wpre[kWarps] = s;
+    }
+    __syncthreads();
+    const int r = sh.wpre[warp] + x - v;
+    if (total) *total = sh.wpre[kWarps];
+    __syncthreads();
+    return r;
+}
+
+// Exact threshold of the k largest of vals[0..n) (ties to the lower index).
+// On return sh.T and sh.jlast describe the selection.
+__device__ void topk_threshold(const float* vals, int n, int k, SelShared& sh, int* err) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float lo = CUDART_INF_F, hi = -CUDART_INF_F;
+    for (int j = tid; j < n; j += kSelThreads) {
+        const float x = vals[j];
+        lo = fminf(lo, x);
+        hi = fmaxf(hi, x);
+    }
+    lo = warp_min(lo);
+    hi = warp_max(hi);
+    if (lane == 0) { sh.red_f[warp] = lo; sh.red_f2[warp] = hi; }
+    for (int b = tid; b < kBins; b += kSelThreads) sh.hist[b] = 0;
+    if (tid == 0) sh.ncand = 0;
+    __syncthreads();
+    if (warp == 0) {
+        lo = warp_min(sh.red_f[lane]);
+        hi = warp_max(sh.red_f2[lane]);
+        if (lane == 0) { sh.vmin = lo; sh.vmax = hi; }
+    }
+    __syncthreads();
+    const float vmin = sh.vmin, vmax = sh.vmax;
+    if (!(vmax > vmin)) {
+        // all scores equal (or not finite): the k lowest indices
+        if (tid == 0) {
+            sh.T = vmax;
+            sh.jlast = k - 1;
+            if (!(vmax == vmax) || isinf(vmax)) set_err(err, DEV_ERR_NUMERIC, 301);
+        }
+        __syncthreads();
+        return;
+    }
+    float invw = static_cast<float>(kBins) / (vmax - vmin);
+    if (!isfinite(invw)) invw = 0.f;
+    for (int j = tid; j < n; j += kSelThreads) atomicAdd(&sh.hist[bin_of(vals[j], vmin, invw)], 1);
+    __syncthreads();
+    // bins 2t, 2t+1 per thread; find the bin holding the k-th largest
+    const int s_t = sh.hist[2 * tid] + sh.hist[2 * tid + 1];
+    int tot = 0;
+    const int pre = block_exscan(s_t, sh, &tot);
+    const int above_t = tot - pre - s_t;   // scores in bins above 2t+1
+    if (above_t < k && k <= above_t + s_t) {
+        const int h1 = sh.hist[2 * tid + 1];
+        if (above_t + h1 >= k) { sh.bstar = 2 * tid + 1; sh.above = above_t; }
+        else { sh.bstar = 2 * tid; sh.above = above_t + h1; }
+    }
+    __syncthreads();
+    const int bstar = sh.bstar, need = k - sh.above, cnt = sh.hist[bstar];
+    if (cnt <= kCand) {
+        for (int j = tid; j < n; j += kSelThreads) {
+            const float x = vals[j];
+            if (bin_of(x, vmin, invw) == bstar) {
+                const int c = atomicAdd(&sh.ncand, 1);
+                if (c < kCand) { sh.cand_v[c] = x; sh.cand_j[c] = j; }
+            }
+        }
+        __syncthreads();
+        const int nc = min(sh.ncand, kCand);
+        if (tid < nc) {
+            const float x = sh.cand_v[tid];
+            const int jx = sh.cand_j[tid];
+            int rank = 0;
+            for (int m = 0; m < nc; ++m) {
+                const float y = sh.cand_v[m];
+                rank += (y > x) || (y == x && sh.cand_j[m] < jx);
+            }
+            if (rank == need - 1) { sh.T = x; sh.jlast = jx; }
+        }
+        __syncthreads();
+        return;
+    }
+    // crowded boundary bin: exact radix select on the order-preserving keys
+    uint32_t prefix = 0, mask = 0;
+    int rem = need;
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        for (int b = tid; b < 256; b += kSelThreads) sh.hist[b] = 0;
+        __syncthreads();
+        for (int j = tid; j < n; j += kSelThreads) {
+            const float x = vals[j];
+            if (bin_of(x, vmin, invw) != bstar) continue;
+            const uint32_t key = ord_key(x);
+            if ((key & mask) == prefix) atomicAdd(&sh.hist[(key >> shift) & 255], 1);
+        }
+        __syncthreads();
+        if (tid == 0) {
+            int c = 0, d = 255;
+            for (; d > 0; --d) {
+                if (c + sh.hist[d] >= rem) break;
+                c += sh.hist[d];
+            }
+            sh.above = c;
+            sh.bstar = d;
+        }
+        __syncthreads();
+        rem -= sh.above;
+        prefix |= static_cast<uint32_t>(sh.bstar) << shift;
+        mask |= 0xFFu << shift;
+        __syncthreads();
+    }
+    const float T = key_to_float(prefix);
+    // jlast: index of the rem-th score equal to T in index order
+    const int seg = ((n + kWarps - 1) / kWarps + 31) & ~31;
+    const int a = warp * seg, e = min(n, a + seg);
+    int c = 0;
+    for (int j = a + lane; j < a + seg; j += 32) {
+        const bool eq = j < e && vals[j] == T;
+        c += __popc(__ballot_sync(0xffffffffu, eq));
+    }
+    int tot2 = 0;
+    const int wbase = block_exscan(lane == 0 ? c : 0, sh, &tot2);
+    const int base0 = __shfl_sync(0xffffffffu, wbase, 0);
+    int run = base0;
+    for (int j = a + lane; j < a + seg; j += 32) {
+        const bool eq = j < e && vals[j] == T;
+        const unsigned bal = __ballot_sync(0xffffffffu, eq);
+        const int r = run + __popc(bal & ((1u << lane) - 1u));
+        if (eq && r == rem - 1) { sh.jlast = j; }
+        run += __popc(bal);
+    }
+    if (tid == 0) sh.T = T;
+    __syncthreads();
+}
+
+// Writes the selected indices (ascending) via out_fn(pos, j); returns the count.
+template <class F>
+__device__ int compact_selected(const float* vals, int n, float T, int jlast, SelShared& sh, F out_fn) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int seg = ((n + kWarps - 1) / kWarps + 31) & ~31;
+    const int a = warp * seg, e = min(n, a + seg);
+    int c = 0;
+    for (int j = a + lane; j < a + seg; j += 32) {
+        bool take = false;
+        if (j < e) { const float x = vals[j]; take = (x > T) || (x == T && j <= jlast); }
+        c += __popc(__ballot_sync(0xffffffffu, take));
+    }
+    int total = 0;
+    const int wb = block_exscan(lane == 0 ? c : 0, sh, &total);
+    int run = __shfl_sync(0xffffffffu, wb, 0);
+    for (int j = a + lane; j < a + seg; j += 32) {
+        bool take = false;
+        if (j < e) { const float x = vals[j]; take = (x > T) || (x == T && j <= jlast); }
+        const unsigned bal = __ballot_sync(0xffffffffu, take);
+        if (take) out_fn(run + __popc(bal & ((1u << lane) - 1u)), j);
+        run += __popc(bal);
+    }
+    __syncthreads();
+    return total;
+}
+
+__device__ __forceinline__ int lower_bound(const int32_t* a, int n, int x) {
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (a[mid] < x) lo = mid + 1; else hi = mid;
+    }
+    return lo;
+}
+
+// ----------------------------------------------------------------- decode
+template <int G>
+__global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
+    extern __shared__ __align__(16) uint8_t dsm[];
+    __shared__ SelShared sh;
+    const int u = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n = p.n, K = p.k;
+    float* vals = (n <= p.smem_cap) ? reinterpret_cast<float*>(dsm) : p.vbuf + static_cast<int64_t>(u) * n;
+    const int cap_f = (n <= p.smem_cap) ? ((n + 3) & ~3) : 0;
+    int32_t* sSel = reinterpret_cast<int32_t*>(dsm) + cap_f;
+    int32_t* sSlot = sSel + K;
+    int32_t* sFree = sSlot + K;
+
+    // 1. log-sum-exp of every query head from the scoring partials
+    if (warp < G) {
+        const int64_t c_first = (static_cast<int64_t>(u) * n) / p.per;
+        const int64_t c_last = (static_cast<int64_t>(u + 1) * n - 1) / p.per;
+        const int64_t nrec = (c_last - c_first + 1) * kScoreWarps;
+        float M = -CUDART_INF_F;
+        for (int64_t r = lane; r < nrec; r += 32) {
+            const int64_t c = c_first + r / kScoreWarps;
+            const int w = static_cast<int>(r % kScoreWarps);
+            const int slot = static_cast<int>(u - (c * p.per) / n);
+            if (c >= p.ncta || slot < 0 || slot >= p.slots) { set_err(p.err, DEV_ERR_BOUNDS, 311); continue; }
+            M = fmaxf(M, p.part[((c * p.slots + slot) * kScoreWarps + w) * G + warp].x);
+        }
+        M = warp_max(M);
+        float S = 0.f;
+        for (int64_t r = lane; r < nrec; r += 32) {
+            const int64_t c = c_first + r / kScoreWarps;
+            const int w = static_cast<int>(r % kScoreWarps);
+            const int slot = static_cast<int>(u - (c * p.per) / n);
+            if (c >= p.ncta || slot < 0 || slot >= p.slots) continue;
+            const float2 ms = p.part[((c * p.slots + slot) * kScoreWarps + w) * G + warp];
+            if (ms.x != -CUDART_INF_F) S += ms.y * __expf(ms.x - M);
+        }
+        S = warp_sum(S);
+        if (lane == 0) sh.lse[warp] = M + __logf(S);
+    }
+    __syncthreads();
+    // 2. v_j = max_g (z_gj - lse_g)
+    float lse[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) lse[g] = sh.lse[g];
+    const float* z = p.logits + static_cast<int64_t>(u) * n * G;
+    for (int j = tid; j < n; j += kSelThreads) {
+        float v = -CUDART_INF_F;
+        if constexpr (G == 4) {
+            const float4 zz = reinterpret_cast<const float4*>(z)[j];
+            v = fmaxf(fmaxf(zz.x - lse[0], zz.y - lse[1]), fmaxf(zz.z - lse[2], zz.w - lse[3]));
+        } else {
+#pragma unroll
+            for (int g = 0; g < G; ++g) v = fmaxf(v, z[static_cast<int64_t>(j) * G + g] - lse[g]);
+        }
+        vals[j] = v;
+    }
+    __syncthreads();
+    // 3. exact top-K threshold and ordered compaction into sSel (original chunk ids)
+    topk_threshold(vals, n, K, sh, p.err);
+    const float T = sh.T;
+    const int jlast = sh.jlast;
+    const int32_t* ids = p.ids + static_cast<int64_t>(u) * n;
+    const int got = compact_selected(vals, n, T, jlast, sh, [&](int pos, int j) {
+        if (pos < K) sSel[pos] = ids[j];
+    });
+    if (got != K) {
+        // only non-finite scores can break the count; keep downstream indices valid
+        if (tid == 0) set_err(p.err, DEV_ERR_NUMERIC, 312);
+        for (int i = tid; i < K; i += kSelThreads) sSel[i] = ids[i];
+        __syncthreads();
+    }
+    // 4. index scan against the previous step's selection
+    const int t = p.t;
+    const int32_t* pids = p.prev_ids + static_cast<int64_t>(u) * K;
+    const int32_t* pslot = p.prev_slot + static_cast<int64_t>(u) * K;
+    for (int i = tid; i < K; i += kSelThreads) {
+        int slot = -1;
+        if (t > 0) {
+            const int pidx = lower_bound(pids, K, sSel[i]);
+            if (pidx < K && pids[pidx] == sSel[i]) {
+                slot = pslot[pidx];
+                if (slot < 0 || slot >= K) { set_err(p.err, DEV_ERR_BOUNDS, 313); slot = -1; }
+            }
+        }
+        sSlot[i] = slot;
+    }
+    __syncthreads();
+    // ordered compaction of misses (by i) and of freed slots (by previous position)
+    constexpr int PER = 4;   // K <= 4096
+    int mflag[PER], fflag[PER], mc = 0, fc = 0;
+#pragma unroll
+    for (int r = 0; r < PER; ++r) {
+        const int i = tid * PER + r;
+        mflag[r] = (i < K) && sSlot[i] < 0;
+        int fr = 0;
+        if (i < K) {
+            if (t == 0) fr = 1;
+            else {
+                const int x = pids[i];
+                const int q = lower_bound(sSel, K, x);
+                fr = !(q < K && sSel[q] == x);
+            }
+        }
+        fflag[r] = fr;
+        mc += mflag[r];
+        fc += fr;
+    }
+    int nmiss = 0, nfree = 0;
+    int mbase = block_exscan(mc, sh, &nmiss);
+    int fbase = block_exscan(fc, sh, &nfree);
+#pragma unroll
+    for (int r = 0; r < PER; ++r) {
+        const int i = tid * PER + r;
+        if (fflag[r]) sFree[fbase++] = (t == 0) ? i : pslot[i];
+    }
+    __syncthreads();
+    if (nmiss != nfree && tid == 0) set_err(p.err, DEV_ERR_BOUNDS, 314);
+    int32_t* cids = p.cur_ids + static_cast<int64_t>(u) * K;
+    int32_t* cslot = p.cur_slot + static_cast<int64_t>(u) * K;
+    int32_t* mch = p.miss_chunk + static_cast<int64_t>(u) * K;
+    int32_t* msl = p.miss_slot + static_cast<int64_t>(u) * K;
+#pragma unroll
+    for (int r = 0; r < PER; ++r) {
+        const int i = tid * PER + r;
+        if (i >= K) continue;
+        int slot = sSlot[i];
+        if (mflag[r]) {
+            const int m = mbase++;
+            slot = (m < nfree) ? sFree[m] : 0;
+            if (slot < 0 || slot >= K) { set_err(p.err, DEV_ERR_BOUNDS, 315); slot = 0; }
+            mch[m] = sSel[i];
+            msl[m] = slot;
+        }
+        cids[i] = sSel[i];
+        cslot[i] = slot;
+        if (p.sel_out_user) p.sel_out_user[static_cast<int64_t>(u) * K + i] = sSel[i];
+    }
+    if (tid == 0) {
+        p.miss_count[u] = nmiss;
+        atomicAdd(p.hits_step + t, K - nmiss);
+    }
+    // 5. append the new token to the exact local set at row W + t
+    const int row = p.W + t;
+    if (row < p.loc_cap) {
+        const int n16 = kD * p.es / 16;
+        const int64_t off = (static_cast<int64_t>(u) * p.loc_cap + row) * kD * p.es;
+        const int64_t src = static_cast<int64_t>(u) * kD * p.es;
+        if (tid < n16)
+            copy_row16(static_cast<uint8_t*>(p.k_loc) + off, static_cast<const uint8_t*>(p.k_new) + src, n16, tid, 1 << 30);
+        else if (tid >= 32 && tid < 32 + n16)
+            copy_row16(static_cast<uint8_t*>(p.v_loc) + off, static_cast<const uint8_t*>(p.v_new) + src, n16, tid - 32,
+                       1 << 30);
+    } else if (tid == 0) {
+        set_err(p.err, DEV_ERR_BOUNDS, 316);
+    }
+}
+
+// ----------------------------------------------------------------- outliers (prefill)
+__global__ void __launch_bounds__(kSelThreads) k_select_outliers(SelectParams p) {
+    extern __shared__ __align__(16) uint8_t dsm[];
+    __shared__ SelShared sh;
+    const int u = blockIdx.x, tid = threadIdx.x;
+    const int n = p.n, k = p.k;
+    float* vals = (n <= p.smem_cap) ? reinterpret_cast<float*>(dsm) : p.vbuf + static_cast<int64_t>(u) * n;
+    const float* src = p.neg_src + static_cast<int64_t>(u) * n;
+    for (int j = tid; j < n; j += kSelThreads) vals[j] = -src[j];
+    __syncthreads();
+    topk_threshold(vals, n, k, sh, p.err);
+    int32_t* out = p.sel_plain + static_cast<int64_t>(u) * k;
+    const int got = compact_selected(vals, n, sh.T, sh.jlast, sh, [&](int pos, int j) {
+        if (pos < k) out[pos] = j;
+    });
+    if (got != k) {
+        if (tid == 0) set_err(p.err, DEV_ERR_NUMERIC, 321);
+        for (int i = tid; i < k; i += kSelThreads) out[i] = i;
+    }
+}
+
+int launch_select_decode(int dtype, const SelectParams& p, cudaStream_t s) {
+    (void)dtype;
+    const int cap_f = (p.n <= p.smem_cap) ? ((p.n + 3) & ~3) : 0;
+    const size_t smem = static_cast<size_t>(cap_f) * 4 + static_cast<size_t>(p.k) * 4 * 3;
+    void (*fn)(SelectParams) = nullptr;
+    switch (p.G) {
+        case 1: fn = k_select_decode<1>; break;
+        case 2: fn = k_select_decode<2>; break;
+        case 4: fn = k_select_decode<4>; break;
+        case 8: fn = k_select_decode<8>; break;
+        default: return -1;
+    }
+    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    fn<<<p.U, kSelThreads, smem, s>>>(p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_select_outliers(const SelectParams& p, cudaStream_t s) {
+    const size_t smem = (p.n <= p.smem_cap) ? static_cast<size_t>((p.n + 3) & ~3) * 4 : 0;
+    cudaFuncSetAttribute(k_select_outliers, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    k_select_outliers<<<p.U, kSelThreads, smem, s>>>(p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace skv

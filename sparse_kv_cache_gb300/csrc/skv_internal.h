@@ -1,0 +1,128 @@
+// Internal types shared by the kernel translation units and the host API.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace skv {
+
+constexpr int kD = 128;        // head dim
+constexpr int kC = 8;          // chunk size
+constexpr int kTileChunks = 16;   // chunks per tensor-core rebuild tile (128 rows)
+constexpr int kSelThreads = 1024;
+constexpr int kAttnSeg = 256;  // tokens per attention CTA
+constexpr int kScoreWarps = 8; // consumer warps of the scoring kernel
+constexpr int kScoreStages = 3;
+constexpr int kScoreStageBytes = 32768;
+
+// Device error word codes (err[0]); err[1] records where the error happened.
+enum : int { DEV_ERR_BOUNDS = 1, DEV_ERR_TIMEOUT = 2, DEV_ERR_NUMERIC = 3 };
+
+// ---------------------------------------------------------------- scoring
+struct ScoreParams {
+    const void* L;        // [U][n_c][d]
+    const void* q;        // [U*G][d]
+    float* logits;        // [U][n_c][G]  z = q.L / sqrt(d)
+    float2* part;         // [ncta][slots][kScoreWarps][G] (max, sum exp(z - max))
+    int n_c;
+    int64_t total;        // U * n_c
+    int64_t per;          // chunks per CTA
+    int slots;            // max units one CTA touches
+    float scale;
+    int* err;
+};
+int launch_score(int dtype, int G, const ScoreParams& p, int ncta, cudaStream_t s);
+int score_ctas_per_sm(int dtype, int G);
+
+// ---------------------------------------------------------------- selection
+struct SelectParams {
+    // top-K over n scores per unit (ties to the lower index), output ascending
+    int n;                // n_c (decode) or candidates (outliers)
+    int k;                // K or O
+    int U, H, G;
+    // decode: scores from logits and score partials
+    const float* logits; const float2* part;
+    int64_t per; int slots; int ncta;
+    // outlier mode: score = -src[u][j]
+    const float* neg_src;
+    float* vbuf;          // [U][n] global score buffer when n exceeds shared memory
+    int smem_cap;         // scores that fit in shared memory
+    // outputs
+    const int32_t* ids;   // [U][n] original chunk id of position j (NULL: identity)
+    int32_t* sel_out_user;   // [U][k] or NULL
+    int32_t* sel_plain;   // [U][k] (outlier mode output)
+    // hit/miss state (decode)
+    int t;
+    int32_t* prev_ids; int32_t* prev_slot;   // [U][K]
+    int32_t* cur_ids; int32_t* cur_slot;     // [U][K]
+    int32_t* miss_chunk; int32_t* miss_slot; int32_t* miss_count;  // [U][K], [U]
+    int32_t* hits_step;   // [max_new_tokens]
+    // append of the new token
+    const void* k_new; const void* v_new; void* k_loc; void* v_loc;
+    int loc_cap; int W; int es;
+    int* err;
+};
+int launch_select_decode(int dtype, const SelectParams& p, cudaStream_t s);
+int launch_select_outliers(const SelectParams& p, cudaStream_t s);
+
+// ---------------------------------------------------------------- rebuild / gather
+struct RebuildParams {
+    int mode;                 // 0: store RoPE'd keys, 1: landmark + min-cos statistics
+    int U, H, r, nkb;
+    int64_t S;
+    int nchunk;               // S / C, bound on chunk ids
+    const int32_t* list;      // [U][list_us] chunk ids, or NULL: chunk = list_base + index
+    int64_t list_us; int list_base; int list_cap;
+    const int32_t* cnt;       // [U] entries, or NULL: count_const
+    int count_const;
+    const int32_t* dst_idx;   // [U][list_us] destination chunk slot, or NULL: index
+    int dst_cap;              // chunk slots per unit in dst
+    void* dst; int64_t dst_us;   // elements per unit of dst
+    float* Lfull; float* mcos; int64_t stats_us;   // [U][stats_us][d], [U][stats_us]
+    const float2* rope_lo;    // [256][d/2] (cos, sin) of lo * theta_i
+    const float2* rope_hi;    // [nhi][d/2] (cos, sin) of hi * 256 * theta_i
+    int nhi;
+    const void* A;            // fp32 path: [b][S][r]
+    const void* B;            // fp32 path: [U][r][d]
+    int* err;
+};
+int launch_rebuild_tc(const CUtensorMap* tmA, const CUtensorMap* tmB, const RebuildParams& p, int grid_x,
+                      cudaStream_t s);
+int launch_rebuild_f32(const RebuildParams& p, int grid_x, cudaStream_t s);
+int launch_transpose_B(const void* B, void* Bt, int U, int r, cudaStream_t s);
+
+struct GatherParams {
+    const void* src; int64_t src_us;   // rows of unit u start at src + u*src_us (elements)
+    const int32_t* list; int64_t list_us; int list_base; int list_cap;
+    const int32_t* cnt; int count_const;
+    const int32_t* dst_idx; int dst_cap;
+    void* dst; int64_t dst_us;
+    int nchunk; int es; int U;
+    int* err;
+};
+int launch_gather(const GatherParams& p, int grid_x, cudaStream_t s);
+
+struct CompactParams {
+    const float* Lfull; int64_t ncand;   // [U][ncand][d]
+    const int32_t* out_ids; int O;       // [U][O] ascending
+    void* L; int32_t* ids; int n_c;      // [U][n_c][d], [U][n_c]
+    int U; int dtype; int* err;
+};
+int launch_compact(const CompactParams& p, cudaStream_t s);
+
+// ---------------------------------------------------------------- attention
+struct AttnParams {
+    const void* q;                 // [U*G][d]
+    const void* k_out; const void* v_out; int n_out;    // [U][n_out][d]
+    const void* k_c; const void* v_c; int n_cache;      // [U][n_cache][d]
+    const void* k_loc; const void* v_loc; int n_loc; int loc_cap;   // [U][loc_cap][d]
+    void* out;                     // [U*G][d]
+    float* part;                   // [U][nsplit][G][d + 4]
+    int* counter;                  // [U]
+    int nsplit; float scale; int G; int U;
+    int* err;
+};
+int launch_attn(int dtype, const AttnParams& p, cudaStream_t s);
+
+}  // namespace skv
