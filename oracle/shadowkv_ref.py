@@ -202,19 +202,33 @@ def attend(q_group: np.ndarray, K: np.ndarray, V: np.ndarray) -> np.ndarray:
     return softmax_rows(s) @ np.asarray(V, np.float64)
 
 
+def round_to_storage(x: np.ndarray, storage: str | None) -> np.ndarray:
+    """Value of x once stored in the configured storage dtype: "bf16" rounds
+    to bfloat16 (nearest even), "f32" to float32, None keeps float64."""
+    if storage is None:
+        return np.asarray(x, np.float64)
+    if storage == "bf16":
+        return bf16_round(x)
+    if storage == "f32":
+        return np.asarray(x, np.float32).astype(np.float64)
+    raise ValueError(storage)
+
+
 def attend_on_index_set(q_group, A_b, B_bh, V_bh, outlier_ids, sel_ids, k_local, v_local,
-                        C: int, base: float) -> np.ndarray:
+                        C: int, base: float, storage: str | None = None) -> np.ndarray:
     """Attention over [K_outlier; RoPE(K_sparse); K_local] for given index sets
     (summary page, "Assembly of the final sparse KV cache").  Keys of outlier
-    and selected chunks are rebuilt here in float64 from A and B."""
+    and selected chunks are rebuilt here in float64 from A and B; with
+    ``storage`` set, the keys the method keeps (outlier keys, rebuilt keys,
+    local-window keys) take the value they have once stored in that dtype."""
     A_b = np.asarray(A_b, np.float64)
     V_bh = np.asarray(V_bh, np.float64)
     to = chunk_tokens(outlier_ids, C)
     ts = chunk_tokens(sel_ids, C)
     d = np.asarray(B_bh).shape[1]
-    K = np.concatenate([rebuild_keys(A_b[to], B_bh, to, base),
-                        rebuild_keys(A_b[ts], B_bh, ts, base),
-                        np.asarray(k_local, np.float64).reshape(-1, d)])
+    K = np.concatenate([round_to_storage(rebuild_keys(A_b[to], B_bh, to, base), storage),
+                        round_to_storage(rebuild_keys(A_b[ts], B_bh, ts, base), storage),
+                        round_to_storage(np.asarray(k_local, np.float64).reshape(-1, d), storage)])
     V = np.concatenate([V_bh[to], V_bh[ts], np.asarray(v_local, np.float64).reshape(-1, d)])
     return attend(q_group, K, V)
 

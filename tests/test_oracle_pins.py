@@ -271,3 +271,21 @@ def test_near_tie_band():
     s = np.array([1.0, 0.5, 0.50004, 0.2, 0.49999])
     band, kth = ref.near_tie_band(s, 2, 1e-4)
     assert kth == 0.50004 and set(band.tolist()) == {1, 2, 4}
+
+
+def test_storage_rounding_of_kept_keys():
+    c = _dense_case(seed=10, steps=1)
+    h, base = 0, 500000.0
+    st = ref.UnitDecodeState(ref.prefill_unit(c["A"], c["Bs"][h], c["V"][h], c["C"], c["O"], c["W"], base))
+    qg = c["qs"][0, :c["G"]]
+    kl = list(st.pre.k_local) + [c["kn"][0, h]]
+    vl = list(st.pre.v_local) + [c["vn"][0, h]]
+    sel = np.arange(5)
+    a = ref.attend_on_index_set(qg, c["A"], c["Bs"][h], c["V"][h], st.pre.outlier_ids, sel, kl, vl, c["C"], base)
+    b = ref.attend_on_index_set(qg, c["A"], c["Bs"][h], c["V"][h], st.pre.outlier_ids, sel, kl, vl, c["C"], base,
+                                storage="f32")
+    d = ref.attend_on_index_set(qg, c["A"], c["Bs"][h], c["V"][h], st.pre.outlier_ids, sel, kl, vl, c["C"], base,
+                                storage="bf16")
+    assert 0 < np.max(np.abs(a - b)) < 1e-5 < np.max(np.abs(a - d)) < 0.1
+    x = np.array([1.0 + 2 ** -9, 3.0, -2.0 ** -130])
+    np.testing.assert_array_equal(ref.round_to_storage(x, "bf16"), ref.bf16_round(x))
