@@ -91,8 +91,13 @@ int shadowkv_validate_config(const skv_config* cfg);
  *
  *   A  dev  [b][S][r]      low-rank token coordinates (borrowed)
  *   B  dev  [b][H][r][d]   per-head bases (borrowed)
- *   V  dev or host [b][H][S][d]  values; host memory must be page-locked
- *      (cudaHostAlloc / cudaHostRegister) when v_place = SKV_V_HOST (borrowed)
+ *   V  dev or host [b][H][S][d]  values (borrowed).  With v_place = SKV_V_HOST
+ *      the GPU reads them in place over the host link: V must be page-locked
+ *      (cudaHostAlloc / cudaHostRegister) or, on a device that reads pageable
+ *      memory through the host's page tables (Grace + NVLink-C2C), any system
+ *      memory -- shadowkv_host_alloc gives huge-page memory for this, whose
+ *      few large translations keep random chunk reads at link speed.
+ *      Otherwise SKV_ERR_NOT_PINNED.
  *
  * A, B and V must stay valid until shadowkv_destroy: decode steps read A/B
  * rows and V rows of the chunks they miss.  The library owns everything else.
@@ -202,6 +207,19 @@ typedef struct {
 } skv_model;
 int shadowkv_model(const skv_config* cfg, double alpha, int64_t t, double b_gpu_gbs,
                    double b_link_gbs, skv_model* out);
+
+/*
+ * Host memory for values read in place by the GPU (v_place = SKV_V_HOST).
+ * Not from the pages: it serves the value offload of the summary page's
+ * section 3.4 ("What gets offloaded to the CPU") on a Grace host, where the
+ * GPU reaches system memory through the CPU's page tables.  Returns memory
+ * aligned to, and advised onto, transparent huge pages (512 MiB on a 64 KiB
+ * page kernel), so that the GPU's translations of a multi-GB value store stay
+ * few.  Pages are populated on first touch.  shadowkv_host_free releases it.
+ * SKV_ERR_INVALID for bytes == 0 or out == NULL, SKV_ERR_OOM on failure.
+ */
+int shadowkv_host_alloc(size_t bytes, void** out);
+void shadowkv_host_free(void* p);
 
 void shadowkv_destroy(skv_layer* layer);   /* frees everything the handle owns; NULL ok */
 const char* shadowkv_strerror(int code);

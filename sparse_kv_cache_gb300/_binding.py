@@ -25,7 +25,7 @@ ERRORS = {0: "OK", -1: "INVALID", -2: "OOM", -3: "NOT_PINNED", -4: "CUDA", -5: "
 EXPORTED = ("shadowkv_validate_config", "shadowkv_prefill_index", "shadowkv_decode_step",
             "shadowkv_stats", "shadowkv_reset_stats", "shadowkv_set_profiling",
             "shadowkv_export_size", "shadowkv_export", "shadowkv_model", "shadowkv_destroy",
-            "shadowkv_strerror", "shadowkv_version")
+            "shadowkv_strerror", "shadowkv_version", "shadowkv_host_alloc", "shadowkv_host_free")
 
 
 class SkvConfig(ctypes.Structure):
@@ -89,6 +89,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.shadowkv_strerror.argtypes = [i32]
     lib.shadowkv_strerror.restype = ctypes.c_char_p
     lib.shadowkv_version.argtypes = []
+    lib.shadowkv_host_alloc.argtypes = [sz, ctypes.POINTER(vp)]
+    lib.shadowkv_host_alloc.restype = i32
+    lib.shadowkv_host_free.argtypes = [vp]
+    lib.shadowkv_host_free.restype = None
     for name in ("shadowkv_validate_config", "shadowkv_prefill_index", "shadowkv_decode_step",
                  "shadowkv_stats", "shadowkv_reset_stats", "shadowkv_set_profiling",
                  "shadowkv_export", "shadowkv_model", "shadowkv_version"):
@@ -140,6 +144,53 @@ def _stream(s) -> int | None:
         import torch
         return torch.cuda.current_stream().cuda_stream
     return s.cuda_stream if hasattr(s, "cuda_stream") else int(s)
+
+
+class HostBuffer:
+    """Huge-page system memory from shadowkv_host_alloc, viewed as a CPU tensor."""
+
+    def __init__(self, shape, dtype):
+        import numpy as np
+        import torch
+        self.shape, self.dtype = tuple(shape), dtype
+        elem = torch.empty((), dtype=dtype).element_size()
+        self.nbytes = int(np.prod(self.shape)) * elem
+        p = ctypes.c_void_p()
+        _check(load().shadowkv_host_alloc(self.nbytes, ctypes.byref(p)), "shadowkv_host_alloc")
+        self._p = p
+        raw = (ctypes.c_uint8 * self.nbytes).from_address(p.value)
+        self.tensor = torch.frombuffer(raw, dtype=torch.uint8).view(dtype).view(self.shape)
+
+    def data_ptr(self) -> int:
+        return self._p.value
+
+    def fill_from(self, src, chunk_bytes: int = 256 << 20):
+        """Copy a same-shaped tensor (any device) in, the host CPU writing every
+        page first (staged through a page-locked buffer for device sources)."""
+        import torch
+        flat_dst = self.tensor.view(-1).view(torch.uint8)
+        flat_src = src.contiguous().view(-1).view(torch.uint8)
+        assert flat_src.numel() == flat_dst.numel()
+        if flat_src.device.type == "cpu":
+            flat_dst.copy_(flat_src)
+            return
+        stage = torch.empty(min(chunk_bytes, flat_dst.numel()), dtype=torch.uint8, pin_memory=True)
+        for off in range(0, flat_dst.numel(), stage.numel()):
+            n = min(stage.numel(), flat_dst.numel() - off)
+            stage[:n].copy_(flat_src[off:off + n])
+            flat_dst[off:off + n].copy_(stage[:n])
+
+    def free(self):
+        if getattr(self, "_p", None) and self._p.value:
+            self.tensor = None
+            load().shadowkv_host_free(self._p)
+            self._p = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
 
 
 class Layer:

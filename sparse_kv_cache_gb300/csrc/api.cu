@@ -8,10 +8,13 @@
 #include <algorithm>
 #include <array>
 #include <cmath>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <new>
 #include <vector>
+
+#include <sys/mman.h>
 
 #include "shadowkv.h"
 #include "skv_internal.h"
@@ -65,8 +68,8 @@ struct skv_layer {
     float2 *rope_lo = nullptr, *rope_hi = nullptr;
     int32_t* hits_step = nullptr;
     int* err = nullptr;
-    CUtensorMap tmA{}, tmB{};
-    int score_ncta = 0, score_slots = 0, sel_smem_cap = 0;
+    CUtensorMap tmA{}, tmB{}, tmL{};
+    int score_ncta = 0, score_slots = 0, score_nparts = 0, sel_smem_cap = 0, fetch_grid = 0;
     int64_t score_per = 0;
     int64_t t = 0, t_reset = 0;
     cudaStream_t last_main = nullptr, last_side = nullptr;
@@ -173,7 +176,7 @@ void step_bytes(const skv_config& c, int64_t t, double misses, double* hbm, doub
     h += (misses > 0 ? U : 0.0) * es * r * d;   // B slices
     double l = misses * C * d * es;             // value rows over the host link
     if (c.v_place == SKV_V_HBM) { h += l; l = 0.0; }
-    const double nsplit = std::ceil((O * C + K * C + loc) / kAttnSeg);
+    const double nsplit = std::ceil((O * C + K * C + loc) / attn_segment(c.dtype));
     *hbm = h;
     *link = l;
     *scratch = U * (2.0 * n_c * G * 4.0 + nsplit * G * (d + 4) * 4.0 * 2.0);
@@ -188,7 +191,7 @@ const char* shadowkv_strerror(int code) {
         case SKV_OK: return "ok";
         case SKV_ERR_INVALID: return "invalid argument or configuration";
         case SKV_ERR_OOM: return "device allocation failed";
-        case SKV_ERR_NOT_PINNED: return "host values are not page-locked";
+        case SKV_ERR_NOT_PINNED: return "host values are not reachable by the GPU (not page-locked, no ATS)";
         case SKV_ERR_CUDA: return "CUDA call failed";
         case SKV_ERR_DEVICE_BOUNDS: return "a kernel met an out-of-range index";
         case SKV_ERR_TIMEOUT: return "a kernel wait timed out";
@@ -295,24 +298,37 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
         if (!is_device_ptr(V)) return fail(SKV_ERR_INVALID);
         h->Vd = V;
     } else {
+        // page-locked host memory (mapped into the GPU's page tables), or, on
+        // a device that reads pageable memory through the host's page tables
+        // (Grace with NVLink-C2C), any system memory, e.g. shadowkv_host_alloc
         cudaPointerAttributes a;
-        if (cudaPointerGetAttributes(&a, V) != cudaSuccess || a.type != cudaMemoryTypeHost) {
+        if (cudaPointerGetAttributes(&a, V) != cudaSuccess) {
             cudaGetLastError();
             return fail(SKV_ERR_NOT_PINNED);
         }
-        void* dp = nullptr;
-        if (cudaHostGetDevicePointer(&dp, const_cast<void*>(V), 0) != cudaSuccess || !dp) {
-            cudaGetLastError();
+        if (a.type == cudaMemoryTypeHost) {
+            void* dp = nullptr;
+            if (cudaHostGetDevicePointer(&dp, const_cast<void*>(V), 0) != cudaSuccess || !dp) {
+                cudaGetLastError();
+                return fail(SKV_ERR_NOT_PINNED);
+            }
+            h->Vd = dp;
+        } else if (a.type == cudaMemoryTypeUnregistered) {
+            int ats = 0;
+            cudaDeviceGetAttribute(&ats, cudaDevAttrPageableMemoryAccessUsesHostPageTables, h->dev);
+            if (!ats) return fail(SKV_ERR_NOT_PINNED);
+            h->Vd = V;
+        } else {
             return fail(SKV_ERR_NOT_PINNED);
         }
-        h->Vd = dp;
     }
 
     const int U = h->U, K = h->K, O = h->O, G = h->G, es = h->es;
     const size_t row = static_cast<size_t>(kD) * es;
     // score work split: every CTA resident in one wave
     {
-        const int tile = kScoreStageBytes / static_cast<int>(row);
+        const int tile = h->dtype == SKV_BF16 ? kScTile : kScoreStageBytes / static_cast<int>(row);
+        h->score_nparts = score_parts(h->dtype);
         const int64_t total = static_cast<int64_t>(U) * h->n_c;
         const int cap = std::max(1, h->sm_count * score_ctas_per_sm(h->dtype, G));
         int64_t ncta = std::min<int64_t>(cap, std::max<int64_t>(1, (total + tile - 1) / tile));
@@ -325,7 +341,9 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
         }
         h->score_slots = slots;
     }
-    h->sel_smem_cap = std::max(0, (200 * 1024 - 12 * K) / 4 - 4);
+    h->sel_smem_cap = std::max(0, (200 * 1024 - 20 * K) / 4 - 4);
+    // value fetch: 4 warps per SM worth of 256-thread CTAs, at most one warp per possible miss
+    h->fetch_grid = static_cast<int>(std::min<int64_t>(h->sm_count / 2 + 1, (static_cast<int64_t>(U) * K + 7) / 8));
 
     const size_t nc = static_cast<size_t>(h->n_c);
     if ((rc = alloc(h, &h->L, U * nc * row)) || (rc = alloc_t(h, &h->ids, U * nc)) ||
@@ -345,7 +363,7 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
         (rc = alloc_t(h, &h->miss_slot, static_cast<size_t>(U) * K)) ||
         (rc = alloc_t(h, &h->miss_count, static_cast<size_t>(U))) ||
         (rc = alloc_t(h, &h->logits, U * nc * G)) ||
-        (rc = alloc_t(h, &h->score_part, static_cast<size_t>(h->score_ncta) * h->score_slots * kScoreWarps * G)) ||
+        (rc = alloc_t(h, &h->score_part, static_cast<size_t>(h->score_ncta) * h->score_slots * h->score_nparts * G)) ||
         (rc = alloc_t(h, &h->vbuf, std::max(U * nc, static_cast<size_t>(U) * h->ncand))) ||
         (rc = alloc_t(h, &h->attn_cnt, static_cast<size_t>(U))) ||
         (rc = alloc_t(h, &h->rope_lo, static_cast<size_t>(256) * kD / 2)) ||
@@ -354,7 +372,8 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
         return fail(rc);
     {
         const int ntot_max = O * kC + K * kC + h->loc_cap;
-        const int nsplit_max = (ntot_max + kAttnSeg - 1) / kAttnSeg;
+        const int seg = attn_segment(h->dtype);
+        const int nsplit_max = (ntot_max + seg - 1) / seg;
         if ((rc = alloc_t(h, &h->attn_part, static_cast<size_t>(U) * nsplit_max * G * (kD + 4)))) return fail(rc);
     }
     void* Lfull = nullptr;
@@ -390,7 +409,8 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
     if (h->dtype == SKV_BF16) {
         if (launch_transpose_B(B, h->Bt, U, h->r, s)) return fail(SKV_ERR_CUDA);
         if ((rc = make_map(&h->tmA, A, h->r, static_cast<uint64_t>(c.batch) * c.seq_len, 8)) ||
-            (rc = make_map(&h->tmB, h->Bt, h->r, static_cast<uint64_t>(U) * kD, 128)))
+            (rc = make_map(&h->tmB, h->Bt, h->r, static_cast<uint64_t>(U) * kD, 128)) ||
+            (rc = make_map(&h->tmL, h->L, kD, static_cast<uint64_t>(U) * h->n_c, kScTile)))
             return fail(rc);
     }
 
@@ -490,14 +510,15 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     ScoreParams sp{};
     sp.L = h->L; sp.q = q; sp.logits = h->logits; sp.part = h->score_part; sp.n_c = h->n_c;
     sp.total = static_cast<int64_t>(U) * h->n_c; sp.per = h->score_per; sp.slots = h->score_slots;
+    sp.nparts = h->score_nparts;
     sp.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(kD))); sp.err = h->err;
-    if (launch_score(h->dtype, G, sp, h->score_ncta, sm)) return SKV_ERR_CUDA;
+    if (launch_score(h->dtype, G, &h->tmL, sp, h->score_ncta, sm)) return SKV_ERR_CUDA;
     if (h->profiling) cudaEventRecord(ev[1], sm);
     // a3 + a4 + a1: top-K, index scan, append
     SelectParams sel{};
     sel.n = h->n_c; sel.k = K; sel.U = U; sel.H = h->H; sel.G = G;
     sel.logits = h->logits; sel.part = h->score_part; sel.per = h->score_per; sel.slots = h->score_slots;
-    sel.ncta = h->score_ncta; sel.vbuf = h->vbuf; sel.smem_cap = h->sel_smem_cap; sel.ids = h->ids;
+    sel.ncta = h->score_ncta; sel.nparts = h->score_nparts; sel.vbuf = h->vbuf; sel.smem_cap = h->sel_smem_cap; sel.ids = h->ids;
     sel.sel_out_user = sel_out; sel.t = t;
     sel.prev_ids = h->sel_ids[t & 1]; sel.prev_slot = h->sel_slot[t & 1];
     sel.cur_ids = h->sel_ids[(t + 1) & 1]; sel.cur_slot = h->sel_slot[(t + 1) & 1];
@@ -516,7 +537,8 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     g.src = h->Vd; g.src_us = h->S * kD; g.list = h->miss_chunk; g.list_us = K; g.list_cap = K;
     g.cnt = h->miss_count; g.dst_idx = h->miss_slot; g.dst_cap = K; g.dst = h->Vc;
     g.dst_us = static_cast<int64_t>(K) * kC * kD; g.nchunk = h->nchunk; g.es = h->es; g.U = U; g.err = h->err;
-    if (launch_gather(g, (K + 7) / 8, ss)) return SKV_ERR_CUDA;
+    const int frc = h->dtype == SKV_BF16 ? launch_fetch(g, h->fetch_grid, ss) : launch_gather(g, (K + 7) / 8, ss);
+    if (frc) return SKV_ERR_CUDA;
     if (h->profiling) cudaEventRecord(ev[6], ss);
     if (ss != sm) cudaEventRecord(h->ev_fetch, ss);
     // a5 on the main stream: rebuild + RoPE of the missed chunks' keys
@@ -536,7 +558,8 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     ap.k_c = h->Kc; ap.v_c = h->Vc; ap.n_cache = K * kC;
     ap.k_loc = h->Kloc; ap.v_loc = h->Vloc; ap.n_loc = h->W + t + 1; ap.loc_cap = h->loc_cap;
     ap.out = out; ap.part = h->attn_part; ap.counter = h->attn_cnt;
-    ap.nsplit = (ap.n_out + ap.n_cache + ap.n_loc + kAttnSeg - 1) / kAttnSeg;
+    const int seg = attn_segment(h->dtype);
+    ap.nsplit = (ap.n_out + ap.n_cache + ap.n_loc + seg - 1) / seg;
     ap.scale = sp.scale; ap.G = G; ap.U = U; ap.err = h->err;
     if (launch_attn(h->dtype, ap, sm)) return SKV_ERR_CUDA;
     if (h->profiling) {
@@ -665,6 +688,25 @@ int shadowkv_export(skv_layer* h, int field, void* dst, size_t bytes, skv_stream
     }
     return SKV_OK;
 }
+
+int shadowkv_host_alloc(size_t bytes, void** out) {
+    if (!out || bytes == 0) return SKV_ERR_INVALID;
+    *out = nullptr;
+    size_t huge = static_cast<size_t>(2) << 20;
+    if (FILE* f = std::fopen("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", "r")) {
+        unsigned long long v = 0;
+        if (std::fscanf(f, "%llu", &v) == 1 && v >= 4096 && (v & (v - 1)) == 0) huge = static_cast<size_t>(v);
+        std::fclose(f);
+    }
+    const size_t n = (bytes + huge - 1) / huge * huge;
+    void* p = nullptr;
+    if (posix_memalign(&p, huge, n) != 0 || !p) return SKV_ERR_OOM;
+    madvise(p, n, MADV_HUGEPAGE);
+    *out = p;
+    return SKV_OK;
+}
+
+void shadowkv_host_free(void* p) { std::free(p); }
 
 void shadowkv_destroy(skv_layer* h) {
     if (!h) return;

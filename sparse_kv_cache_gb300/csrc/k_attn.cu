@@ -178,6 +178,210 @@ __global__ void __launch_bounds__(256) k_attn(AttnParams p) {
     if (tid == 0) p.counter[u] = 0;
 }
 
+// ------------------------------------------------------------------ bf16: bulk-staged variant
+// One thread issues 1-D bulk copies (TMA engine) of the CTA's key rows and
+// value rows (at most three contiguous pieces: outliers, cache slots, local)
+// into shared memory, completion counted on two mbarriers, so every byte of
+// the CTA is in flight at once and the values arrive while the scores are
+// being computed.  128 tokens per CTA, 4 warps, 3 CTAs per SM.
+constexpr int kBSeg = 128;
+
+template <int G>
+__global__ void __launch_bounds__(128) k_attn_bulk(AttnParams p) {
+    extern __shared__ __align__(128) uint8_t smb[];
+    uint8_t* sK = smb;                                   // [128][128] bf16, then the reduction buffer
+    uint8_t* sV = smb + kBSeg * kD * 2;                  // [128][128] bf16
+    float* sS = reinterpret_cast<float*>(smb + 2 * kBSeg * kD * 2);   // [128][G]
+    __shared__ uint64_t barK, barV;
+    __shared__ float red_m[4][G], red_l[4][G];
+    __shared__ int s_last, s_fail;
+
+    const int u = blockIdx.y, split = blockIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, hl = lane & 15, half = lane >> 4;
+    const int ntot = p.n_out + p.n_cache + p.n_loc;
+    const int seg0 = split * kBSeg;
+    const int nseg = min(kBSeg, ntot - seg0);
+
+    if (tid == 0) {
+        mbar_init(&barK, 1);
+        mbar_init(&barV, 1);
+        s_fail = 0;
+        fence_mbar_init();
+        const uint32_t bytes = static_cast<uint32_t>(max(nseg, 0)) * kD * 2;
+        mbar_arrive_expect_tx(&barK, bytes);
+        mbar_arrive_expect_tx(&barV, bytes);
+        // pieces of [seg0, seg0 + nseg) in the three regions
+        const int bounds[4] = {0, p.n_out, p.n_out + p.n_cache, ntot};
+        for (int r = 0; r < 3; ++r) {
+            const int a = max(seg0, bounds[r]), b = min(seg0 + nseg, bounds[r + 1]);
+            if (a >= b) continue;
+            const __nv_bfloat16 *kb, *vb;
+            if (r == 0) {
+                kb = static_cast<const __nv_bfloat16*>(p.k_out) + (static_cast<int64_t>(u) * p.n_out + a) * kD;
+                vb = static_cast<const __nv_bfloat16*>(p.v_out) + (static_cast<int64_t>(u) * p.n_out + a) * kD;
+            } else if (r == 1) {
+                kb = static_cast<const __nv_bfloat16*>(p.k_c) + (static_cast<int64_t>(u) * p.n_cache + a - bounds[1]) * kD;
+                vb = static_cast<const __nv_bfloat16*>(p.v_c) + (static_cast<int64_t>(u) * p.n_cache + a - bounds[1]) * kD;
+            } else {
+                kb = static_cast<const __nv_bfloat16*>(p.k_loc) + (static_cast<int64_t>(u) * p.loc_cap + a - bounds[2]) * kD;
+                vb = static_cast<const __nv_bfloat16*>(p.v_loc) + (static_cast<int64_t>(u) * p.loc_cap + a - bounds[2]) * kD;
+            }
+            const uint32_t nb = static_cast<uint32_t>(b - a) * kD * 2;
+            bulk_g2s(sK + (a - seg0) * kD * 2, kb, nb, &barK);
+            bulk_g2s(sV + (a - seg0) * kD * 2, vb, nb, &barV);
+        }
+    }
+    float qv[G][8];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+        load8(static_cast<const __nv_bfloat16*>(p.q) + (static_cast<int64_t>(u) * G + g) * kD + hl * 8, qv[g]);
+    __syncthreads();
+    if (!mbar_wait(&barK, 0)) { set_err(p.err, DEV_ERR_TIMEOUT, 601); s_fail = 1; }
+
+    // ---- scores: warp w owns tokens [32w, 32w+32), a half-warp per token row
+#pragma unroll
+    for (int round = 0; round < 2; ++round) {
+        const int tb = warp * 32 + round * 16 + half * 8;
+        float acc[G][8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            float v[8];
+            if (tb + c < nseg) {
+                load8(reinterpret_cast<const __nv_bfloat16*>(sK + (tb + c) * kD * 2) + hl * 8, v);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) v[k] = 0.f;
+            }
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float a = 0.f;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) a = fmaf(qv[g][k], v[k], a);
+                acc[g][c] = a;
+            }
+        }
+        float sc[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) sc[g] = transpose_reduce8(acc[g], hl) * p.scale;
+        const int tl = tb + (hl >> 1);
+        if ((hl & 1) == 0) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) sS[tl * G + g] = tl < nseg ? sc[g] : -CUDART_INF_F;
+        }
+    }
+    __syncthreads();
+    float M[G], Lsum[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const float x = warp_max(sS[tid * G + g]);
+        if (lane == 0) red_m[warp][g] = x;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const float x = fmaxf(fmaxf(red_m[0][g], red_m[1][g]), fmaxf(red_m[2][g], red_m[3][g]));
+        M[g] = x;
+        const float sv = sS[tid * G + g];
+        const float pv = (sv == -CUDART_INF_F) ? 0.f : __expf(sv - x);
+        sS[tid * G + g] = pv;
+        const float ws = warp_sum(pv);
+        if (lane == 0) red_l[warp][g] = ws;
+    }
+    if (!mbar_wait(&barV, 0)) { set_err(p.err, DEV_ERR_TIMEOUT, 602); s_fail = 1; }
+    __syncthreads();
+#pragma unroll
+    for (int g = 0; g < G; ++g) Lsum[g] = red_l[0][g] + red_l[1][g] + red_l[2][g] + red_l[3][g];
+
+    // ---- p . V: 8 half-warps, 16 tokens each, lane owns 8 dims
+    const int hw = warp * 2 + half;
+    float acc[G][8];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[g][k] = 0.f;
+#pragma unroll 4
+    for (int tl = hw; tl < nseg; tl += 8) {
+        float v[8];
+        load8(reinterpret_cast<const __nv_bfloat16*>(sV + tl * kD * 2) + hl * 8, v);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const float pg = sS[tl * G + g];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc[g][k] = fmaf(pg, v[k], acc[g][k]);
+        }
+    }
+    float* sRed = reinterpret_cast<float*>(sK);          // keys are no longer needed
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        float* r = sRed + (hw * G + g) * kD + hl * 8;
+        reinterpret_cast<float4*>(r)[0] = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
+        reinterpret_cast<float4*>(r)[1] = make_float4(acc[g][4], acc[g][5], acc[g][6], acc[g][7]);
+    }
+    __syncthreads();
+    float* mypart = p.part + (static_cast<int64_t>(u) * p.nsplit + split) * G * kPartPitch;
+    for (int o = tid; o < G * kD; o += 128) {
+        float x = 0.f;
+#pragma unroll
+        for (int h = 0; h < 8; ++h) x += sRed[h * G * kD + o];
+        const int g = o / kD, dim = o % kD;
+        mypart[g * kPartPitch + dim] = x;
+        if (dim == 0) {
+            mypart[g * kPartPitch + kD] = M[g];
+            mypart[g * kPartPitch + kD + 1] = Lsum[g];
+        }
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = (atomicAdd(p.counter + u, 1) == p.nsplit - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    // merge: (max, sum) of every split into shared memory, the weights once per
+    // (split, head), then the accumulators with independent loads in flight
+    const float* parts = p.part + static_cast<int64_t>(u) * p.nsplit * G * kPartPitch;
+    float* sW = sS;                                   // [nsplit][G] weights (sS is free now)
+    float* sMl = sS + p.nsplit * G;                   // [nsplit][G] (max, sum) pairs
+    for (int i = tid; i < p.nsplit * G; i += 128) {
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(parts + i * kPartPitch + kD));
+        sW[i] = ml.x;
+        sMl[i] = ml.y;
+    }
+    __syncthreads();
+    if (tid < G) {
+        float mx = -CUDART_INF_F;
+        for (int sp = 0; sp < p.nsplit; ++sp) mx = fmaxf(mx, sW[sp * G + tid]);
+        float ls = 0.f;
+        for (int sp = 0; sp < p.nsplit; ++sp) {
+            const float m = sW[sp * G + tid];
+            const float w = (m == -CUDART_INF_F) ? 0.f : __expf(m - mx);
+            sW[sp * G + tid] = w;
+            ls = fmaf(sMl[sp * G + tid], w, ls);
+        }
+        for (int sp = 0; sp < p.nsplit; ++sp) sW[sp * G + tid] /= ls;
+    }
+    __syncthreads();
+    for (int o = tid; o < G * kD; o += 128) {
+        const int g = o / kD, dim = o % kD;
+        float a = 0.f;
+#pragma unroll 8
+        for (int sp = 0; sp < p.nsplit; ++sp) a = fmaf(__ldcg(parts + (sp * G + g) * kPartPitch + dim), sW[sp * G + g], a);
+        static_cast<__nv_bfloat16*>(p.out)[(static_cast<int64_t>(u) * G + g) * kD + dim] = __float2bfloat16_rn(a);
+    }
+    if (tid == 0) p.counter[u] = 0;
+}
+
+template <int G>
+static int launch_bulk(const AttnParams& p, cudaStream_t s) {
+    const size_t scores = static_cast<size_t>(kBSeg) * G * 4;
+    const size_t merge = static_cast<size_t>(2) * p.nsplit * G * 4;
+    const size_t smem = static_cast<size_t>(2) * kBSeg * kD * 2 + (scores > merge ? scores : merge);
+    cudaFuncSetAttribute(k_attn_bulk<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    k_attn_bulk<G><<<dim3(p.nsplit, p.U), 128, smem, s>>>(p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+int attn_segment(int dtype) { return dtype == 1 ? kBSeg : kAttnSeg; }
+
 template <typename T, int G>
 static int launch_t(const AttnParams& p, cudaStream_t s) {
     const size_t smem = (static_cast<size_t>(kAttnSeg) * G + 16 * G * kD) * 4;
@@ -189,10 +393,10 @@ static int launch_t(const AttnParams& p, cudaStream_t s) {
 int launch_attn(int dtype, const AttnParams& p, cudaStream_t s) {
     if (dtype == 1) {
         switch (p.G) {
-            case 1: return launch_t<__nv_bfloat16, 1>(p, s);
-            case 2: return launch_t<__nv_bfloat16, 2>(p, s);
-            case 4: return launch_t<__nv_bfloat16, 4>(p, s);
-            case 8: return launch_t<__nv_bfloat16, 8>(p, s);
+            case 1: return launch_bulk<1>(p, s);
+            case 2: return launch_bulk<2>(p, s);
+            case 4: return launch_bulk<4>(p, s);
+            case 8: return launch_bulk<8>(p, s);
         }
     } else {
         switch (p.G) {

@@ -46,6 +46,54 @@ __global__ void __launch_bounds__(256) k_gather(GatherParams p) {
     }
 }
 
+// Decode-time value fetch.  Over NVLink-C2C the latency of a host read is
+// long, so bandwidth needs many chunks in flight at once: every warp fetches
+// four 2 KB chunks of one unit (16 loads of 16 bytes per lane in flight), a
+// CTA covers 32 misses, and the grid covers every possible miss, so all of a
+// step's misses are requested together while each CTA stays small enough to
+// share SMs with the concurrent key rebuild.  bf16 rows of 128 values only.
+__global__ void __launch_bounds__(256) k_fetch(GatherParams p) {
+    const int u = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = (blockIdx.x * 8 + warp) * 4;
+    const int cnt = p.cnt[u];
+    if (cnt < 0 || cnt > p.list_cap) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) set_err(p.err, DEV_ERR_BOUNDS, 503);
+        return;
+    }
+    if (m0 >= cnt) return;
+    uint4 r[4][4];
+    uint4* dst[4] = {nullptr, nullptr, nullptr, nullptr};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int m = m0 + k;
+        if (m >= cnt) continue;
+        const int ch = p.list[u * p.list_us + m];
+        const int sl = p.dst_idx[u * p.list_us + m];
+        if (ch < 0 || ch >= p.nchunk || sl < 0 || sl >= p.dst_cap) {
+            if (lane == 0) set_err(p.err, DEV_ERR_BOUNDS, 504);
+            continue;
+        }
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.src) +
+                                                          (u * p.src_us + static_cast<int64_t>(ch) * kC * kD) * 2);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) r[k][q] = src[lane + 32 * q];
+        dst[k] = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.dst) + (u * p.dst_us + static_cast<int64_t>(sl) * kC * kD) * 2);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        if (dst[k])
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dst[k][lane + 32 * q] = r[k][q];
+}
+
+int launch_fetch(const GatherParams& p, int grid, cudaStream_t s) {
+    (void)grid;
+    const int gx = (p.list_cap + 31) / 32;
+    if (gx <= 0) return 0;
+    k_fetch<<<dim3(gx, p.U), 256, 0, s>>>(p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
 int launch_gather(const GatherParams& p, int grid_x, cudaStream_t s) {
     if (grid_x <= 0) return 0;
     k_gather<<<dim3(grid_x, p.U), 256, 0, s>>>(p);

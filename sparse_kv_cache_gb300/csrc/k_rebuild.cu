@@ -17,10 +17,13 @@
 //    memory; the four warps read their 32 rows back with tcgen05.ld.
 //  * fp32: CUDA-core FMAs, one thread per row, B broadcast from shared memory
 //    (tf32 tensor cores would not meet fp32 accuracy).
-// Epilogue (both): RoPE with angles composed from two tables,
-// cos/sin(pos*theta) = product of the (pos & 255) and (pos >> 8)*256 entries,
-// built on the host in double precision; then either the bf16/fp32 key rows
-// go to their destination slot, or the statistics are formed in fp32.
+// Epilogue (both): the fp32 tile is staged in shared memory (the operand
+// buffers, free once the MMAs retire), then RoPE runs one warp per row with
+// angles composed from two tables, cos/sin(pos*theta) from the (pos & 255)
+// and (pos >> 8)*256 entries built on the host in double precision, so every
+// table read and key store is contiguous across the warp; then either the
+// bf16/fp32 key rows go to their destination slot, or the statistics are
+// formed in fp32.
 #include <math_constants.h>
 
 #include "skv_common.cuh"
@@ -36,46 +39,80 @@ struct TileInfo {
     int dst;     // destination chunk slot
 };
 
-__device__ __forceinline__ void rope_pair(const RebuildParams& p, int pos, int i, float& a, float& b) {
-    const float2 lo = p.rope_lo[(pos & 255) * (kD / 2) + i];
-    const float2 hi = p.rope_hi[(pos >> 8) * (kD / 2) + i];
-    const float c = hi.x * lo.x - hi.y * lo.y;
-    const float s = hi.y * lo.x + hi.x * lo.y;
-    const float x = a, y = b;
-    a = x * c - y * s;
-    b = x * s + y * c;
+// Stage one row half (dims [32h, 32h+32) and [64+32h, +32)) of raw fp32 keys.
+__device__ __forceinline__ void stage_half(float* stage, int row, int h, const float (&v0)[32], const float (&v1)[32]) {
+    float* srow = stage + row * kStagePitch;
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+        *reinterpret_cast<float4*>(srow + 32 * h + i) = make_float4(v0[i], v0[i + 1], v0[i + 2], v0[i + 3]);
+        *reinterpret_cast<float4*>(srow + kD / 2 + 32 * h + i) = make_float4(v1[i], v1[i + 1], v1[i + 2], v1[i + 3]);
+    }
 }
 
-// Rotate one row half (dims [32h, 32h+32) and [64+32h, 64+32h+32)) and store it.
+// RoPE over the staged tile.  Warp w owns chunks w, w+4, w+8, w+12; for a
+// chunk it holds the (cos, sin) table entries of all 8 rows (one `hi` entry,
+// shared by the chunk since 8-aligned chunks never straddle a 256 boundary,
+// and 8 `lo` entries), fetched ahead with all loads in flight.  Lane l
+// rotates the pairs (2l, 2l+64) and (2l+1, 2l+65), so table reads,
+// shared-memory reads and the row stores are contiguous across the warp.  The
+// angle of position pos is composed from the (pos & 255) and (pos >> 8)
+// tables by the addition formulas.  Mode 0 stores the rotated rows into their
+// slot; mode 1 writes them back into the staging tile for the statistics.
+struct RopeRegs {
+    float4 lo[kC];
+    float4 hi;
+};
+
+__device__ __forceinline__ void rope_fetch(const RebuildParams& p, const TileInfo& t, RopeRegs& r) {
+    const int lane = threadIdx.x & 31;
+    if (t.chunk < 0) return;
+    const int pos0 = t.chunk * kC;
+    r.hi = reinterpret_cast<const float4*>(p.rope_hi + (pos0 >> 8) * (kD / 2))[lane];
+#pragma unroll
+    for (int i = 0; i < kC; ++i) r.lo[i] = reinterpret_cast<const float4*>(p.rope_lo + ((pos0 + i) & 255) * (kD / 2))[lane];
+}
+
 template <typename OutT>
-__device__ __forceinline__ void finish_half(const RebuildParams& p, int u, int row, const TileInfo& ti, int h,
-                                            float (&v0)[32], float (&v1)[32], float* stage) {
-    const bool valid = ti.chunk >= 0;
-    const int pos = valid ? ti.chunk * kC + (row & 7) : 0;
-    if (valid) {
+__device__ __forceinline__ void rope_chunk(const RebuildParams& p, int u, int c, const TileInfo& t, const RopeRegs& r,
+                                           float* stage) {
+    const int lane = threadIdx.x & 31;
+    if (t.chunk < 0) return;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) rope_pair(p, pos, 32 * h + i, v0[i], v1[i]);
-    }
-    if (p.mode == 0) {
-        if (!valid) return;
-        OutT* dst = static_cast<OutT*>(p.dst) + u * p.dst_us + (static_cast<int64_t>(ti.dst) * kC + (row & 7)) * kD;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            float w[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) w[k] = v0[8 * q + k];
-            store8(dst + 32 * h + 8 * q, w);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) w[k] = v1[8 * q + k];
-            store8(dst + kD / 2 + 32 * h + 8 * q, w);
-        }
-    } else {
+    for (int i = 0; i < kC; ++i) {
+        const int row = c * kC + i;
+        const float4 lo = r.lo[i], hi = r.hi;
+        const float c0 = hi.x * lo.x - hi.y * lo.y, s0 = hi.y * lo.x + hi.x * lo.y;
+        const float c1 = hi.z * lo.z - hi.w * lo.w, s1 = hi.w * lo.z + hi.z * lo.w;
         float* srow = stage + row * kStagePitch;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            srow[32 * h + i] = v0[i];
-            srow[kD / 2 + 32 * h + i] = v1[i];
+        const float2 a = *reinterpret_cast<const float2*>(srow + 2 * lane);
+        const float2 b = *reinterpret_cast<const float2*>(srow + kD / 2 + 2 * lane);
+        const float2 ra = make_float2(a.x * c0 - b.x * s0, a.y * c1 - b.y * s1);
+        const float2 rb = make_float2(a.x * s0 + b.x * c0, a.y * s1 + b.y * c1);
+        if (p.mode == 0) {
+            OutT* dst = static_cast<OutT*>(p.dst) + u * p.dst_us + (static_cast<int64_t>(t.dst) * kC + i) * kD;
+            if constexpr (sizeof(OutT) == 2) {
+                reinterpret_cast<uint32_t*>(dst)[lane] = pack_bf16x2(ra.x, ra.y);
+                reinterpret_cast<uint32_t*>(dst + kD / 2)[lane] = pack_bf16x2(rb.x, rb.y);
+            } else {
+                reinterpret_cast<float2*>(dst)[lane] = ra;
+                reinterpret_cast<float2*>(dst + kD / 2)[lane] = rb;
+            }
+        } else {
+            *reinterpret_cast<float2*>(srow + 2 * lane) = ra;
+            *reinterpret_cast<float2*>(srow + kD / 2 + 2 * lane) = rb;
         }
+    }
+}
+
+// All chunks of the tile; `first` holds the prefetched entries of the warp's first chunk.
+template <typename OutT>
+__device__ void rope_tile(const RebuildParams& p, int u, const TileInfo* ti, float* stage, const RopeRegs& first) {
+    const int warp = threadIdx.x >> 5;
+    rope_chunk<OutT>(p, u, warp, ti[warp], first, stage);
+    for (int c = warp + 4; c < kTileChunks; c += 4) {
+        RopeRegs r;
+        rope_fetch(p, ti[c], r);
+        rope_chunk<OutT>(p, u, c, ti[c], r, stage);
     }
 }
 
@@ -217,6 +254,8 @@ __global__ void __launch_bounds__(128, 1) k_rebuild_tc(const __grid_constant__ C
         }
     }
     __syncthreads();
+    RopeRegs first;
+    rope_fetch(p, ti[warp], first);   // table loads in flight while the MMAs run
     bool ok = !s_fail;
     if (ok && !mbar_wait(&bar_mma, 0)) {
         set_err(p.err, DEV_ERR_TIMEOUT, 412);
@@ -228,7 +267,6 @@ __global__ void __launch_bounds__(128, 1) k_rebuild_tc(const __grid_constant__ C
     float* stage = reinterpret_cast<float*>(smem);            // reused once the MMAs are done
     float* smean = stage + kRows * kStagePitch;
     const int row = tid;
-    const TileInfo mine = ti[row >> 3];
     if (ok) {
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
 #pragma unroll 1
@@ -237,12 +275,18 @@ __global__ void __launch_bounds__(128, 1) k_rebuild_tc(const __grid_constant__ C
             tmem_ld32(lane_base + 32 * h, v0);
             tmem_ld32(lane_base + kD / 2 + 32 * h, v1);
             tmem_ld_wait();
-            finish_half<OutT>(p, u, row, mine, h, v0, v1, stage);
+            stage_half(stage, row, h, v0, v1);
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (ok && p.mode == 1) tile_stats(p, u, ti, stage, smean);
+    if (ok) {
+        rope_tile<OutT>(p, u, ti, stage, first);
+        if (p.mode == 1) {
+            __syncthreads();
+            tile_stats(p, u, ti, stage, smean);
+        }
+    }
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, 128);
@@ -290,10 +334,16 @@ __global__ void __launch_bounds__(128) k_rebuild_f32(RebuildParams p) {
         float v0[32], v1[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) { v0[i] = acc[32 * h + i]; v1[i] = acc[kD / 2 + 32 * h + i]; }
-        finish_half<float>(p, u, row, mine, h, v0, v1, stage);
+        stage_half(stage, row, h, v0, v1);
     }
     __syncthreads();
-    if (p.mode == 1) tile_stats(p, u, ti, stage, smean);
+    RopeRegs first;
+    rope_fetch(p, ti[threadIdx.x >> 5], first);
+    rope_tile<float>(p, u, ti, stage, first);
+    if (p.mode == 1) {
+        __syncthreads();
+        tile_stats(p, u, ti, stage, smean);
+    }
 }
 
 // ------------------------------------------------------------------ B transpose (bf16)

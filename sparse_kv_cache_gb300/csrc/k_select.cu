@@ -86,14 +86,9 @@ __device__ int block_exscan(int v, SelShared& sh, int* total) {
 
 // Exact threshold of the k largest of vals[0..n) (ties to the lower index).
 // On return sh.T and sh.jlast describe the selection.
-__device__ void topk_threshold(const float* vals, int n, int k, SelShared& sh, int* err) {
+// lo/hi: this thread's partial min/max of the scores (from the pass that wrote them).
+__device__ void topk_threshold(const float* vals, int n, int k, SelShared& sh, int* err, float lo, float hi) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    float lo = CUDART_INF_F, hi = -CUDART_INF_F;
-    for (int j = tid; j < n; j += kSelThreads) {
-        const float x = vals[j];
-        lo = fminf(lo, x);
-        hi = fmaxf(hi, x);
-    }
     lo = warp_min(lo);
     hi = warp_max(hi);
     if (lane == 0) { sh.red_f[warp] = lo; sh.red_f2[warp] = hi; }
@@ -119,17 +114,31 @@ __device__ void topk_threshold(const float* vals, int n, int k, SelShared& sh, i
     }
     float invw = static_cast<float>(kBins) / (vmax - vmin);
     if (!isfinite(invw)) invw = 0.f;
+#pragma unroll 4
     for (int j = tid; j < n; j += kSelThreads) atomicAdd(&sh.hist[bin_of(vals[j], vmin, invw)], 1);
     __syncthreads();
-    // bins 2t, 2t+1 per thread; find the bin holding the k-th largest
-    const int s_t = sh.hist[2 * tid] + sh.hist[2 * tid + 1];
-    int tot = 0;
-    const int pre = block_exscan(s_t, sh, &tot);
-    const int above_t = tot - pre - s_t;   // scores in bins above 2t+1
-    if (above_t < k && k <= above_t + s_t) {
-        const int h1 = sh.hist[2 * tid + 1];
-        if (above_t + h1 >= k) { sh.bstar = 2 * tid + 1; sh.above = above_t; }
-        else { sh.bstar = 2 * tid; sh.above = above_t + h1; }
+    // one warp finds the bin holding the k-th largest: lane l owns bins [64l, 64l+64)
+    if (warp == 0) {
+        constexpr int per = kBins / 32;
+        int cnt = 0;
+#pragma unroll 8
+        for (int b = 0; b < per; ++b) cnt += sh.hist[lane * per + b];
+        int incl = cnt;   // inclusive suffix sum over lanes >= this one
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_down_sync(0xffffffffu, incl, o);
+            if (lane + o < 32) incl += y;
+        }
+        int above = incl - cnt;   // scores in bins of higher lanes
+        if (above < k && k <= incl) {
+            int b = lane * per + per - 1;
+            for (; b > lane * per; --b) {
+                if (above + sh.hist[b] >= k) break;
+                above += sh.hist[b];
+            }
+            sh.bstar = b;
+            sh.above = above;
+        }
     }
     __syncthreads();
     const int bstar = sh.bstar, need = k - sh.above, cnt = sh.hist[bstar];
@@ -256,28 +265,54 @@ __global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
     int32_t* sSel = reinterpret_cast<int32_t*>(dsm) + cap_f;
     int32_t* sSlot = sSel + K;
     int32_t* sFree = sSlot + K;
+    int32_t* sPid = sFree + K;       // previous step's selection (ascending) ...
+    int32_t* sPslot = sPid + K;      // ... and its slots
+    if (warp >= G) {
+        // work with no dependency on the scores, done while warps < G form the log-sum-exp
+        const int wt = tid - G * 32, nt = kSelThreads - G * 32;
+        if (p.t > 0) {
+            const int32_t* gp = p.prev_ids + static_cast<int64_t>(u) * K;
+            const int32_t* gs = p.prev_slot + static_cast<int64_t>(u) * K;
+            for (int i = wt; i < K; i += nt) { sPid[i] = gp[i]; sPslot[i] = gs[i]; }
+        }
+        // append the new token to the exact local set at row W + t
+        const int row = p.W + p.t;
+        const int n16 = kD * p.es / 16;
+        if (row < p.loc_cap) {
+            const int64_t off = (static_cast<int64_t>(u) * p.loc_cap + row) * kD * p.es;
+            const int64_t src = static_cast<int64_t>(u) * kD * p.es;
+            if (wt < n16)
+                copy_row16(static_cast<uint8_t*>(p.k_loc) + off, static_cast<const uint8_t*>(p.k_new) + src, n16, wt, 1 << 30);
+            else if (wt >= 64 && wt < 64 + n16)
+                copy_row16(static_cast<uint8_t*>(p.v_loc) + off, static_cast<const uint8_t*>(p.v_new) + src, n16, wt - 64,
+                           1 << 30);
+        } else if (wt == 0) {
+            set_err(p.err, DEV_ERR_BOUNDS, 316);
+        }
+    }
 
     // 1. log-sum-exp of every query head from the scoring partials
     if (warp < G) {
         const int64_t c_first = (static_cast<int64_t>(u) * n) / p.per;
         const int64_t c_last = (static_cast<int64_t>(u + 1) * n - 1) / p.per;
-        const int64_t nrec = (c_last - c_first + 1) * kScoreWarps;
+        const int np = p.nparts;
+        const int64_t nrec = (c_last - c_first + 1) * np;
         float M = -CUDART_INF_F;
         for (int64_t r = lane; r < nrec; r += 32) {
-            const int64_t c = c_first + r / kScoreWarps;
-            const int w = static_cast<int>(r % kScoreWarps);
+            const int64_t c = c_first + r / np;
+            const int w = static_cast<int>(r % np);
             const int slot = static_cast<int>(u - (c * p.per) / n);
             if (c >= p.ncta || slot < 0 || slot >= p.slots) { set_err(p.err, DEV_ERR_BOUNDS, 311); continue; }
-            M = fmaxf(M, p.part[((c * p.slots + slot) * kScoreWarps + w) * G + warp].x);
+            M = fmaxf(M, p.part[((c * p.slots + slot) * np + w) * G + warp].x);
         }
         M = warp_max(M);
         float S = 0.f;
         for (int64_t r = lane; r < nrec; r += 32) {
-            const int64_t c = c_first + r / kScoreWarps;
-            const int w = static_cast<int>(r % kScoreWarps);
+            const int64_t c = c_first + r / np;
+            const int w = static_cast<int>(r % np);
             const int slot = static_cast<int>(u - (c * p.per) / n);
             if (c >= p.ncta || slot < 0 || slot >= p.slots) continue;
-            const float2 ms = p.part[((c * p.slots + slot) * kScoreWarps + w) * G + warp];
+            const float2 ms = p.part[((c * p.slots + slot) * np + w) * G + warp];
             if (ms.x != -CUDART_INF_F) S += ms.y * __expf(ms.x - M);
         }
         S = warp_sum(S);
@@ -289,20 +324,43 @@ __global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
 #pragma unroll
     for (int g = 0; g < G; ++g) lse[g] = sh.lse[g];
     const float* z = p.logits + static_cast<int64_t>(u) * n * G;
-    for (int j = tid; j < n; j += kSelThreads) {
-        float v = -CUDART_INF_F;
-        if constexpr (G == 4) {
-            const float4 zz = reinterpret_cast<const float4*>(z)[j];
-            v = fmaxf(fmaxf(zz.x - lse[0], zz.y - lse[1]), fmaxf(zz.z - lse[2], zz.w - lse[3]));
-        } else {
+    float lo = CUDART_INF_F, hi = -CUDART_INF_F;
+    if constexpr (G == 4) {
+        // four independent 16-byte loads in flight per thread
+        const float4* z4 = reinterpret_cast<const float4*>(z);
+        int j = tid;
+        for (; j + 7 * kSelThreads < n; j += 8 * kSelThreads) {
+            float4 a[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) a[r] = __ldcg(z4 + j + r * kSelThreads);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const float v = fmaxf(fmaxf(a[r].x - lse[0], a[r].y - lse[1]), fmaxf(a[r].z - lse[2], a[r].w - lse[3]));
+                vals[j + r * kSelThreads] = v;
+                lo = fminf(lo, v);
+                hi = fmaxf(hi, v);
+            }
+        }
+        for (; j < n; j += kSelThreads) {
+            const float4 zz = __ldcg(z4 + j);
+            const float v = fmaxf(fmaxf(zz.x - lse[0], zz.y - lse[1]), fmaxf(zz.z - lse[2], zz.w - lse[3]));
+            vals[j] = v;
+            lo = fminf(lo, v);
+            hi = fmaxf(hi, v);
+        }
+    } else {
+#pragma unroll 4
+        for (int j = tid; j < n; j += kSelThreads) {
+            float v = -CUDART_INF_F;
 #pragma unroll
             for (int g = 0; g < G; ++g) v = fmaxf(v, z[static_cast<int64_t>(j) * G + g] - lse[g]);
+            vals[j] = v;
+            lo = fminf(lo, v);
+            hi = fmaxf(hi, v);
         }
-        vals[j] = v;
     }
-    __syncthreads();
     // 3. exact top-K threshold and ordered compaction into sSel (original chunk ids)
-    topk_threshold(vals, n, K, sh, p.err);
+    topk_threshold(vals, n, K, sh, p.err, lo, hi);
     const float T = sh.T;
     const int jlast = sh.jlast;
     const int32_t* ids = p.ids + static_cast<int64_t>(u) * n;
@@ -317,8 +375,8 @@ __global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
     }
     // 4. index scan against the previous step's selection
     const int t = p.t;
-    const int32_t* pids = p.prev_ids + static_cast<int64_t>(u) * K;
-    const int32_t* pslot = p.prev_slot + static_cast<int64_t>(u) * K;
+    const int32_t* pids = sPid;
+    const int32_t* pslot = sPslot;
     for (int i = tid; i < K; i += kSelThreads) {
         int slot = -1;
         if (t > 0) {
@@ -351,9 +409,10 @@ __global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
         mc += mflag[r];
         fc += fr;
     }
-    int nmiss = 0, nfree = 0;
-    int mbase = block_exscan(mc, sh, &nmiss);
-    int fbase = block_exscan(fc, sh, &nfree);
+    int both = 0;
+    const int bb = block_exscan(mc | (fc << 16), sh, &both);
+    int mbase = bb & 0xFFFF, fbase = bb >> 16;
+    const int nmiss = both & 0xFFFF, nfree = both >> 16;
 #pragma unroll
     for (int r = 0; r < PER; ++r) {
         const int i = tid * PER + r;
@@ -385,20 +444,6 @@ __global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
         p.miss_count[u] = nmiss;
         atomicAdd(p.hits_step + t, K - nmiss);
     }
-    // 5. append the new token to the exact local set at row W + t
-    const int row = p.W + t;
-    if (row < p.loc_cap) {
-        const int n16 = kD * p.es / 16;
-        const int64_t off = (static_cast<int64_t>(u) * p.loc_cap + row) * kD * p.es;
-        const int64_t src = static_cast<int64_t>(u) * kD * p.es;
-        if (tid < n16)
-            copy_row16(static_cast<uint8_t*>(p.k_loc) + off, static_cast<const uint8_t*>(p.k_new) + src, n16, tid, 1 << 30);
-        else if (tid >= 32 && tid < 32 + n16)
-            copy_row16(static_cast<uint8_t*>(p.v_loc) + off, static_cast<const uint8_t*>(p.v_new) + src, n16, tid - 32,
-                       1 << 30);
-    } else if (tid == 0) {
-        set_err(p.err, DEV_ERR_BOUNDS, 316);
-    }
 }
 
 // ----------------------------------------------------------------- outliers (prefill)
@@ -409,9 +454,14 @@ __global__ void __launch_bounds__(kSelThreads) k_select_outliers(SelectParams p)
     const int n = p.n, k = p.k;
     float* vals = (n <= p.smem_cap) ? reinterpret_cast<float*>(dsm) : p.vbuf + static_cast<int64_t>(u) * n;
     const float* src = p.neg_src + static_cast<int64_t>(u) * n;
-    for (int j = tid; j < n; j += kSelThreads) vals[j] = -src[j];
-    __syncthreads();
-    topk_threshold(vals, n, k, sh, p.err);
+    float lo = CUDART_INF_F, hi = -CUDART_INF_F;
+    for (int j = tid; j < n; j += kSelThreads) {
+        const float v = -src[j];
+        vals[j] = v;
+        lo = fminf(lo, v);
+        hi = fmaxf(hi, v);
+    }
+    topk_threshold(vals, n, k, sh, p.err, lo, hi);
     int32_t* out = p.sel_plain + static_cast<int64_t>(u) * k;
     const int got = compact_selected(vals, n, sh.T, sh.jlast, sh, [&](int pos, int j) {
         if (pos < k) out[pos] = j;
@@ -425,7 +475,7 @@ __global__ void __launch_bounds__(kSelThreads) k_select_outliers(SelectParams p)
 int launch_select_decode(int dtype, const SelectParams& p, cudaStream_t s) {
     (void)dtype;
     const int cap_f = (p.n <= p.smem_cap) ? ((p.n + 3) & ~3) : 0;
-    const size_t smem = static_cast<size_t>(cap_f) * 4 + static_cast<size_t>(p.k) * 4 * 3;
+    const size_t smem = static_cast<size_t>(cap_f) * 4 + static_cast<size_t>(p.k) * 4 * 5;
     void (*fn)(SelectParams) = nullptr;
     switch (p.G) {
         case 1: fn = k_select_decode<1>; break;

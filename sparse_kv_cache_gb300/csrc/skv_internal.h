@@ -20,20 +20,29 @@ constexpr int kScoreStageBytes = 32768;
 enum : int { DEV_ERR_BOUNDS = 1, DEV_ERR_TIMEOUT = 2, DEV_ERR_NUMERIC = 3 };
 
 // ---------------------------------------------------------------- scoring
+// tensor-core scoring (bf16): 128-chunk tiles, 6-stage TMA ring, 4 epilogue warps
+constexpr int kScTile = 128;
+constexpr int kScStages = 6;
+constexpr int kScN = 16;          // MMA N: the G <= 8 query heads, zero-padded
+constexpr int kScParts = 4;       // partial records per (CTA, unit): one per epilogue warp
+
 struct ScoreParams {
     const void* L;        // [U][n_c][d]
     const void* q;        // [U*G][d]
     float* logits;        // [U][n_c][G]  z = q.L / sqrt(d)
-    float2* part;         // [ncta][slots][kScoreWarps][G] (max, sum exp(z - max))
+    float2* part;         // [ncta][slots][nparts][G] (max, sum exp(z - max))
     int n_c;
     int64_t total;        // U * n_c
     int64_t per;          // chunks per CTA
     int slots;            // max units one CTA touches
+    int nparts;           // partial records per (CTA, unit)
     float scale;
     int* err;
 };
-int launch_score(int dtype, int G, const ScoreParams& p, int ncta, cudaStream_t s);
+// bf16: tcgen05 kernel through the tensor map of L; fp32: CUDA-core kernel
+int launch_score(int dtype, int G, const CUtensorMap* tmL, const ScoreParams& p, int ncta, cudaStream_t s);
 int score_ctas_per_sm(int dtype, int G);
+int score_parts(int dtype);
 
 // ---------------------------------------------------------------- selection
 struct SelectParams {
@@ -43,7 +52,7 @@ struct SelectParams {
     int U, H, G;
     // decode: scores from logits and score partials
     const float* logits; const float2* part;
-    int64_t per; int slots; int ncta;
+    int64_t per; int slots; int ncta; int nparts;
     // outlier mode: score = -src[u][j]
     const float* neg_src;
     float* vbuf;          // [U][n] global score buffer when n exceeds shared memory
@@ -102,6 +111,7 @@ struct GatherParams {
     int* err;
 };
 int launch_gather(const GatherParams& p, int grid_x, cudaStream_t s);
+int launch_fetch(const GatherParams& p, int grid, cudaStream_t s);   // bf16 decode misses
 
 struct CompactParams {
     const float* Lfull; int64_t ncand;   // [U][ncand][d]
@@ -124,5 +134,6 @@ struct AttnParams {
     int* err;
 };
 int launch_attn(int dtype, const AttnParams& p, cudaStream_t s);
+int attn_segment(int dtype);   // tokens per attention CTA
 
 }  // namespace skv

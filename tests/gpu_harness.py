@@ -41,7 +41,7 @@ class LayerRun:
     """One layer on the GPU plus lazily computed oracle state per unit."""
 
     def __init__(self, w: Workload, steps: int, gen_device: str = "cpu", layer: int = 0,
-                 side_stream: bool = True):
+                 side_stream: bool = True, host_alloc: str = "pinned"):
         self.w, self.steps = w, steps
         dev = torch.device("cuda")
         A = make_A(w, layer, gen_device)
@@ -49,7 +49,12 @@ class LayerRun:
         V = make_V(w, layer, gen_device)
         q, kn, vn = make_decode_inputs(w, layer, steps, gen_device)
         self.A_d, self.B_d = A.to(dev), B.to(dev)
-        if w.v_place == "host":
+        if w.v_place == "host" and host_alloc == "huge":
+            self.V_buf = skv.HostBuffer(V.shape, V.dtype)   # system memory read through ATS
+            self.V_buf.fill_from(V)
+            self.V_arg = self.V_buf
+            self.V_cpu = self.V_buf.tensor
+        elif w.v_place == "host":
             self.V_arg = V.to("cpu").pin_memory()
             self.V_cpu = self.V_arg
         else:
@@ -261,8 +266,8 @@ def _local_keys(run: LayerRun, u: int, A, B):
 
 
 def run_and_check(w: Workload, steps: int, units=None, gen_device="cpu", check_cache=True,
-                  side_stream=True) -> Report:
-    run = LayerRun(w, steps, gen_device=gen_device, side_stream=side_stream)
+                  side_stream=True, host_alloc="pinned") -> Report:
+    run = LayerRun(w, steps, gen_device=gen_device, side_stream=side_stream, host_alloc=host_alloc)
     units = list(range(w.units)) if units is None else list(units)
     check_prefill(run, units)
     rep = Report()

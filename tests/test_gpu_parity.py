@@ -39,6 +39,11 @@ def test_bf16_host_pinned_values():
     run_and_check(SMALL_BF16.with_(v_place="host", seed=12), 5)
 
 
+def test_bf16_host_huge_page_values():
+    # system memory from shadowkv_host_alloc, read by the GPU through the host page tables
+    run_and_check(SMALL_BF16.with_(v_place="host", seed=14), 4, host_alloc="huge")
+
+
 def test_full_budget_selects_every_chunk():
     w = SMALL_BF16.with_(seq_len=1024, n_outlier=4, batch=1, seed=13)
     w = w.with_(n_select=w.n_selectable)
