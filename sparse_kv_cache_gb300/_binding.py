@@ -147,7 +147,7 @@ def _stream(s) -> int | None:
 
 
 class HostBuffer:
-    """Huge-page system memory from shadowkv_host_alloc, viewed as a CPU tensor."""
+    """Page-locked host memory from shadowkv_host_alloc, viewed as a CPU tensor."""
 
     def __init__(self, shape, dtype):
         import numpy as np
@@ -164,21 +164,17 @@ class HostBuffer:
     def data_ptr(self) -> int:
         return self._p.value
 
-    def fill_from(self, src, chunk_bytes: int = 256 << 20):
-        """Copy a same-shaped tensor (any device) in, the host CPU writing every
-        page first (staged through a page-locked buffer for device sources)."""
-        import torch
-        flat_dst = self.tensor.view(-1).view(torch.uint8)
-        flat_src = src.contiguous().view(-1).view(torch.uint8)
-        assert flat_src.numel() == flat_dst.numel()
-        if flat_src.device.type == "cpu":
-            flat_dst.copy_(flat_src)
-            return
-        stage = torch.empty(min(chunk_bytes, flat_dst.numel()), dtype=torch.uint8, pin_memory=True)
-        for off in range(0, flat_dst.numel(), stage.numel()):
-            n = min(stage.numel(), flat_dst.numel() - off)
-            stage[:n].copy_(flat_src[off:off + n])
-            flat_dst[off:off + n].copy_(stage[:n])
+    def fill_from(self, src, offset_elems: int = 0):
+        """Copy a tensor (any device) into the buffer starting at element offset_elems."""
+        flat = self.tensor.view(-1)
+        s = src.contiguous().view(-1)
+        flat[offset_elems:offset_elems + s.numel()].copy_(s)
+
+    def slice(self, offset_elems: int, shape):
+        """A view of part of the buffer (data_ptr() gives its address)."""
+        import numpy as np
+        n = int(np.prod(shape))
+        return self.tensor.view(-1)[offset_elems:offset_elems + n].view(*shape)
 
     def free(self):
         if getattr(self, "_p", None) and self._p.value:

@@ -14,7 +14,6 @@
 #include <new>
 #include <vector>
 
-#include <sys/mman.h>
 
 #include "shadowkv.h"
 #include "skv_internal.h"
@@ -69,8 +68,8 @@ struct skv_layer {
     int32_t* hits_step = nullptr;
     int* err = nullptr;
     CUtensorMap tmA{}, tmB{}, tmL{};
-    int score_ncta = 0, score_slots = 0, score_nparts = 0, sel_smem_cap = 0, fetch_grid = 0;
-    int64_t score_per = 0;
+    int score_ncta = 0, score_nru = 0, score_nparts = 0, sel_smem_cap = 0;
+    int32_t* sched = nullptr;
     int64_t t = 0, t_reset = 0;
     cudaStream_t last_main = nullptr, last_side = nullptr;
     bool stepped = false;
@@ -325,25 +324,15 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
 
     const int U = h->U, K = h->K, O = h->O, G = h->G, es = h->es;
     const size_t row = static_cast<size_t>(kD) * es;
-    // score work split: every CTA resident in one wave
+    // scoring work: runs of kRunChunks landmarks of one unit; every CTA resident at once
     {
-        const int tile = h->dtype == SKV_BF16 ? kScTile : kScoreStageBytes / static_cast<int>(row);
         h->score_nparts = score_parts(h->dtype);
-        const int64_t total = static_cast<int64_t>(U) * h->n_c;
+        h->score_nru = (h->n_c + kRunChunks - 1) / kRunChunks;
+        const int64_t runs = static_cast<int64_t>(U) * h->score_nru;
         const int cap = std::max(1, h->sm_count * score_ctas_per_sm(h->dtype, G));
-        int64_t ncta = std::min<int64_t>(cap, std::max<int64_t>(1, (total + tile - 1) / tile));
-        h->score_per = (total + ncta - 1) / ncta;
-        h->score_ncta = static_cast<int>((total + h->score_per - 1) / h->score_per);
-        int slots = 1;
-        for (int64_t cta = 0; cta < h->score_ncta; ++cta) {
-            const int64_t a = cta * h->score_per, b = std::min(total, a + h->score_per) - 1;
-            slots = std::max<int>(slots, static_cast<int>(b / h->n_c - a / h->n_c + 1));
-        }
-        h->score_slots = slots;
+        h->score_ncta = static_cast<int>(std::min<int64_t>(cap, runs));
     }
     h->sel_smem_cap = std::max(0, (200 * 1024 - 20 * K) / 4 - 4);
-    // value fetch: 4 warps per SM worth of 256-thread CTAs, at most one warp per possible miss
-    h->fetch_grid = static_cast<int>(std::min<int64_t>(h->sm_count / 2 + 1, (static_cast<int64_t>(U) * K + 7) / 8));
 
     const size_t nc = static_cast<size_t>(h->n_c);
     if ((rc = alloc(h, &h->L, U * nc * row)) || (rc = alloc_t(h, &h->ids, U * nc)) ||
@@ -363,7 +352,8 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
         (rc = alloc_t(h, &h->miss_slot, static_cast<size_t>(U) * K)) ||
         (rc = alloc_t(h, &h->miss_count, static_cast<size_t>(U))) ||
         (rc = alloc_t(h, &h->logits, U * nc * G)) ||
-        (rc = alloc_t(h, &h->score_part, static_cast<size_t>(h->score_ncta) * h->score_slots * h->score_nparts * G)) ||
+        (rc = alloc_t(h, &h->score_part, static_cast<size_t>(U) * h->score_nru * h->score_nparts * G)) ||
+        (rc = alloc_t(h, &h->sched, 1)) ||
         (rc = alloc_t(h, &h->vbuf, std::max(U * nc, static_cast<size_t>(U) * h->ncand))) ||
         (rc = alloc_t(h, &h->attn_cnt, static_cast<size_t>(U))) ||
         (rc = alloc_t(h, &h->rope_lo, static_cast<size_t>(256) * kD / 2)) ||
@@ -406,6 +396,7 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
     cudaMemsetAsync(h->attn_cnt, 0, U * sizeof(int32_t), s);
     cudaMemsetAsync(h->hits_step, 0, h->Tmax * sizeof(int32_t), s);
     cudaMemsetAsync(h->miss_count, 0, U * sizeof(int32_t), s);
+    cudaMemsetAsync(h->sched, 0, sizeof(int32_t), s);
     if (h->dtype == SKV_BF16) {
         if (launch_transpose_B(B, h->Bt, U, h->r, s)) return fail(SKV_ERR_CUDA);
         if ((rc = make_map(&h->tmA, A, h->r, static_cast<uint64_t>(c.batch) * c.seq_len, 8)) ||
@@ -509,16 +500,15 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     // a2: landmark scoring
     ScoreParams sp{};
     sp.L = h->L; sp.q = q; sp.logits = h->logits; sp.part = h->score_part; sp.n_c = h->n_c;
-    sp.total = static_cast<int64_t>(U) * h->n_c; sp.per = h->score_per; sp.slots = h->score_slots;
-    sp.nparts = h->score_nparts;
+    sp.nru = h->score_nru; sp.total_runs = U * h->score_nru; sp.nparts = h->score_nparts; sp.sched = h->sched;
     sp.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(kD))); sp.err = h->err;
     if (launch_score(h->dtype, G, &h->tmL, sp, h->score_ncta, sm)) return SKV_ERR_CUDA;
     if (h->profiling) cudaEventRecord(ev[1], sm);
     // a3 + a4 + a1: top-K, index scan, append
     SelectParams sel{};
     sel.n = h->n_c; sel.k = K; sel.U = U; sel.H = h->H; sel.G = G;
-    sel.logits = h->logits; sel.part = h->score_part; sel.per = h->score_per; sel.slots = h->score_slots;
-    sel.ncta = h->score_ncta; sel.nparts = h->score_nparts; sel.vbuf = h->vbuf; sel.smem_cap = h->sel_smem_cap; sel.ids = h->ids;
+    sel.logits = h->logits; sel.part = h->score_part; sel.nru = h->score_nru; sel.nparts = h->score_nparts;
+    sel.sched = h->sched; sel.vbuf = h->vbuf; sel.smem_cap = h->sel_smem_cap; sel.ids = h->ids;
     sel.sel_out_user = sel_out; sel.t = t;
     sel.prev_ids = h->sel_ids[t & 1]; sel.prev_slot = h->sel_slot[t & 1];
     sel.cur_ids = h->sel_ids[(t + 1) & 1]; sel.cur_slot = h->sel_slot[(t + 1) & 1];
@@ -537,7 +527,7 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     g.src = h->Vd; g.src_us = h->S * kD; g.list = h->miss_chunk; g.list_us = K; g.list_cap = K;
     g.cnt = h->miss_count; g.dst_idx = h->miss_slot; g.dst_cap = K; g.dst = h->Vc;
     g.dst_us = static_cast<int64_t>(K) * kC * kD; g.nchunk = h->nchunk; g.es = h->es; g.U = U; g.err = h->err;
-    const int frc = h->dtype == SKV_BF16 ? launch_fetch(g, h->fetch_grid, ss) : launch_gather(g, (K + 7) / 8, ss);
+    const int frc = launch_gather(g, (K + 7) / 8, ss);
     if (frc) return SKV_ERR_CUDA;
     if (h->profiling) cudaEventRecord(ev[6], ss);
     if (ss != sm) cudaEventRecord(h->ev_fetch, ss);
@@ -692,21 +682,18 @@ int shadowkv_export(skv_layer* h, int field, void* dst, size_t bytes, skv_stream
 int shadowkv_host_alloc(size_t bytes, void** out) {
     if (!out || bytes == 0) return SKV_ERR_INVALID;
     *out = nullptr;
-    size_t huge = static_cast<size_t>(2) << 20;
-    if (FILE* f = std::fopen("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", "r")) {
-        unsigned long long v = 0;
-        if (std::fscanf(f, "%llu", &v) == 1 && v >= 4096 && (v & (v - 1)) == 0) huge = static_cast<size_t>(v);
-        std::fclose(f);
-    }
-    const size_t n = (bytes + huge - 1) / huge * huge;
     void* p = nullptr;
-    if (posix_memalign(&p, huge, n) != 0 || !p) return SKV_ERR_OOM;
-    madvise(p, n, MADV_HUGEPAGE);
+    if (cudaHostAlloc(&p, bytes, cudaHostAllocPortable | cudaHostAllocMapped) != cudaSuccess || !p) {
+        cudaGetLastError();
+        return SKV_ERR_OOM;
+    }
     *out = p;
     return SKV_OK;
 }
 
-void shadowkv_host_free(void* p) { std::free(p); }
+void shadowkv_host_free(void* p) {
+    if (p) cudaFreeHost(p);
+}
 
 void shadowkv_destroy(skv_layer* h) {
     if (!h) return;

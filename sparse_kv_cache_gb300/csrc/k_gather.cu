@@ -3,11 +3,14 @@
 // ShadowKV (English summary, section 3.4, "Fetching values from the CPU": for
 // each missed chunk the C value rows are transferred into the GPU cache;
 // Chinese digest section A2, Algorithm 2: V_sparse = Gather(V_CPU, I)).  With
-// values in page-locked Grace memory the GPU reads them directly over
-// NVLink-C2C (zero-copy loads, one warp per 2 KB chunk), on its own stream so
-// that the transfer overlaps the key rebuild.  The same kernel gathers the
-// outlier chunks' and the local window's values during pre-filling
-// (Algorithm 1: K_outlier, V_outlier = Gather(K_RoPE, V, I)).
+// values in page-locked Grace memory the GPU reads them in place over
+// NVLink-C2C, on its own stream so that the transfer overlaps the key rebuild.
+// A host read has a long latency, so bandwidth needs every missed chunk in
+// flight at once: one warp per chunk (2 KB in bf16, four 16-byte loads per
+// lane issued before the first store), a grid covering every possible miss,
+// no shared memory and few registers, so the rebuild's CTAs fit beside it.
+// The same kernel gathers the outlier chunks' and the local window's values
+// during pre-filling (Algorithm 1: K_outlier, V_outlier = Gather(K_RoPE, V, I)).
 //
 // Pre-filling compaction: L = C \ Gather(C, I) (Algorithm 1, last line).  The
 // landmark of candidate chunk j lands at position j - #{outliers < j}.
@@ -44,54 +47,6 @@ __global__ void __launch_bounds__(256) k_gather(GatherParams p) {
     } else {
         for (int i = lane; i < n16; i += 32) d4[i] = s4[i];
     }
-}
-
-// Decode-time value fetch.  Over NVLink-C2C the latency of a host read is
-// long, so bandwidth needs many chunks in flight at once: every warp fetches
-// four 2 KB chunks of one unit (16 loads of 16 bytes per lane in flight), a
-// CTA covers 32 misses, and the grid covers every possible miss, so all of a
-// step's misses are requested together while each CTA stays small enough to
-// share SMs with the concurrent key rebuild.  bf16 rows of 128 values only.
-__global__ void __launch_bounds__(256) k_fetch(GatherParams p) {
-    const int u = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = (blockIdx.x * 8 + warp) * 4;
-    const int cnt = p.cnt[u];
-    if (cnt < 0 || cnt > p.list_cap) {
-        if (threadIdx.x == 0 && blockIdx.x == 0) set_err(p.err, DEV_ERR_BOUNDS, 503);
-        return;
-    }
-    if (m0 >= cnt) return;
-    uint4 r[4][4];
-    uint4* dst[4] = {nullptr, nullptr, nullptr, nullptr};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int m = m0 + k;
-        if (m >= cnt) continue;
-        const int ch = p.list[u * p.list_us + m];
-        const int sl = p.dst_idx[u * p.list_us + m];
-        if (ch < 0 || ch >= p.nchunk || sl < 0 || sl >= p.dst_cap) {
-            if (lane == 0) set_err(p.err, DEV_ERR_BOUNDS, 504);
-            continue;
-        }
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.src) +
-                                                          (u * p.src_us + static_cast<int64_t>(ch) * kC * kD) * 2);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) r[k][q] = src[lane + 32 * q];
-        dst[k] = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.dst) + (u * p.dst_us + static_cast<int64_t>(sl) * kC * kD) * 2);
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-        if (dst[k])
-#pragma unroll
-            for (int q = 0; q < 4; ++q) dst[k][lane + 32 * q] = r[k][q];
-}
-
-int launch_fetch(const GatherParams& p, int grid, cudaStream_t s) {
-    (void)grid;
-    const int gx = (p.list_cap + 31) / 32;
-    if (gx <= 0) return 0;
-    k_fetch<<<dim3(gx, p.U), 256, 0, s>>>(p);
-    return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
 int launch_gather(const GatherParams& p, int grid_x, cudaStream_t s) {

@@ -5,20 +5,26 @@
 // Selection", Step 1.  This is the largest HBM stream of a decode step: every
 // selectable landmark row (d values) is read once per step.
 //
+// Work is cut into runs of kRunChunks landmarks of one unit.  Each run leaves,
+// besides z = P / sqrt(d) as fp32 [U][n_c][G], one record per part (warp) and
+// query head: the running (max z, sum exp(z - max)), from which the next
+// kernel forms every head's log-sum-exp without a second pass over z.
+//
 // bf16 storage (k_score_tc): the contraction runs on the 5th-generation tensor
-// cores so that the kernel is bound by the landmark stream alone.  Per CTA one
-// warp streams 128-landmark tiles (two 64-column, 128-byte-swizzled boxes,
-// 32 KB) with 2-D TMA copies into a 6-stage shared-memory ring; one thread
-// issues tcgen05 MMAs, M = 128 landmarks x N = 16 (the unit's G <= 8 queries,
-// zero-padded) x K = 128, into a double-buffered fp32 accumulator in tensor
-// memory; four epilogue warps read one landmark row each per thread, scale by
-// 1/sqrt(d), store z and keep the running (max, sum exp) per query head.
+// cores so that the kernel is bound by the landmark stream alone.  A
+// persistent CTA per SM claims runs from an atomic counter (fast SMs take more
+// runs; the tail is one run).  One warp streams 128-landmark tiles (two
+// 64-column, 128-byte-swizzled boxes, 32 KB) with 2-D TMA copies into a
+// 6-stage shared-memory ring; one thread issues tcgen05 MMAs, M = 128
+// landmarks x N = 16 (the unit's G <= 8 queries; the other columns are never
+// read) x K = 128, into a double-buffered fp32 accumulator in tensor memory;
+// four epilogue warps read one landmark row each per thread, scale, store z
+// and keep the running (max, sum exp) per head.  Every stage carries its own
+// copy of the run's query rows, written by the producer warp from registers,
+// so runs of different units follow each other without any drain.
 // fp32 storage (k_score): CUDA-core dot products, the query in registers, one
-// half-warp per landmark row and a transpose-reduction of the partial sums.
-// Outputs: z = P / sqrt(d) as fp32 [U][n_c][G], and per (CTA, unit, part, g)
-// the running (max z, sum exp(z - max)) so the next kernel can form the
-// log-sum-exp of every query head.  The flat chunk range U*n_c is split evenly
-// over at most (SMs x resident CTAs) CTAs, so every CTA is resident at once.
+// half-warp per landmark row and a transpose-reduction of the partial sums;
+// runs are dealt round-robin to the CTAs.
 #include <math_constants.h>
 
 #include "skv_common.cuh"
@@ -26,6 +32,7 @@
 
 namespace skv {
 
+// ------------------------------------------------------------------ CUDA-core path
 template <typename T, int G>
 __global__ void __launch_bounds__((kScoreWarps + 1) * 32) k_score(ScoreParams p) {
     constexpr int ROWB = kD * Elem<T>::bytes;
@@ -36,8 +43,6 @@ __global__ void __launch_bounds__((kScoreWarps + 1) * 32) k_score(ScoreParams p)
     __shared__ volatile int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * p.per;
-    const int64_t c1 = min(c0 + p.per, p.total);
     if (tid == 0) {
         for (int s = 0; s < kScoreStages; ++s) {
             mbar_init(&full[s], 1);
@@ -47,7 +52,6 @@ __global__ void __launch_bounds__((kScoreWarps + 1) * 32) k_score(ScoreParams p)
         fence_mbar_init();
     }
     __syncthreads();
-    if (c0 >= c1) return;
     const int64_t n_c = p.n_c;
 
     if (warp == kScoreWarps) {
@@ -55,11 +59,12 @@ __global__ void __launch_bounds__((kScoreWarps + 1) * 32) k_score(ScoreParams p)
         if (lane != 0) return;
         int it = 0;
         bool ok = true;
-        for (int64_t pos = c0; ok && pos < c1;) {
-            const int64_t u = pos / n_c;
-            const int64_t uend = min(c1, (u + 1) * n_c);
-            for (int64_t j = pos; j < uend; j += TILE, ++it) {
-                const int nv = static_cast<int>(min(static_cast<int64_t>(TILE), uend - j));
+        for (int r = blockIdx.x; ok && r < p.total_runs; r += gridDim.x) {
+            const int64_t u = r / p.nru;
+            const int64_t a = u * n_c + static_cast<int64_t>(r % p.nru) * kRunChunks;
+            const int64_t e = min(a + kRunChunks, (u + 1) * n_c);
+            for (int64_t j = a; j < e; j += TILE, ++it) {
+                const int nv = static_cast<int>(min(static_cast<int64_t>(TILE), e - j));
                 const int s = it % kScoreStages;
                 if (it >= kScoreStages && !mbar_wait(&empty[s], ((it / kScoreStages) - 1) & 1)) {
                     set_err(p.err, DEV_ERR_TIMEOUT, 101);
@@ -72,7 +77,6 @@ __global__ void __launch_bounds__((kScoreWarps + 1) * 32) k_score(ScoreParams p)
                 bulk_g2s(smem + s * kScoreStageBytes, static_cast<const uint8_t*>(p.L) + j * ROWB,
                          static_cast<uint32_t>(nv * ROWB), &full[s]);
             }
-            pos = uend;
         }
         if (!ok) {
             // leave no copy in flight: wait (bounded) for the stages issued last
@@ -85,19 +89,20 @@ __global__ void __launch_bounds__((kScoreWarps + 1) * 32) k_score(ScoreParams p)
     // ---------------------------------------------------- consumers
     const int hl = lane & 15, half = lane >> 4;
     float qv[G][8];
-    int it = 0, slot = 0;
+    int it = 0;
     bool ok = true;
-    for (int64_t pos = c0; pos < c1; ++slot) {
-        const int64_t u = pos / n_c;
-        const int64_t uend = min(c1, (u + 1) * n_c);
+    for (int r = blockIdx.x; ok && r < p.total_runs; r += gridDim.x) {
+        const int64_t u = r / p.nru;
+        const int64_t a = u * n_c + static_cast<int64_t>(r % p.nru) * kRunChunks;
+        const int64_t e = min(a + kRunChunks, (u + 1) * n_c);
 #pragma unroll
         for (int g = 0; g < G; ++g) load8(static_cast<const T*>(p.q) + (u * G + g) * kD + hl * 8, qv[g]);
         float m[G], sx[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) { m[g] = -CUDART_INF_F; sx[g] = 0.f; }
 
-        for (int64_t j = pos; ok && j < uend; j += TILE, ++it) {
-            const int nv = static_cast<int>(min(static_cast<int64_t>(TILE), uend - j));
+        for (int64_t j = a; ok && j < e; j += TILE, ++it) {
+            const int nv = static_cast<int>(min(static_cast<int64_t>(TILE), e - j));
             const int s = it % kScoreStages;
             if (s_abort || !mbar_wait(&full[s], (it / kScoreStages) & 1)) {
                 set_err(p.err, DEV_ERR_TIMEOUT, 102);
@@ -120,10 +125,10 @@ __global__ void __launch_bounds__((kScoreWarps + 1) * 32) k_score(ScoreParams p)
                     }
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
-                        float a = 0.f;
+                        float acc1 = 0.f;
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) a = fmaf(qv[g][k], v[k], a);
-                        acc[g][c] = a;
+                        for (int k = 0; k < 8; ++k) acc1 = fmaf(qv[g][k], v[k], acc1);
+                        acc[g][c] = acc1;
                     }
                 }
                 float z[G];
@@ -132,12 +137,8 @@ __global__ void __launch_bounds__((kScoreWarps + 1) * 32) k_score(ScoreParams p)
                 const int cj = cb + (hl >> 1);
                 if ((hl & 1) == 0 && cj < nv) {
                     float* dst = p.logits + (j + cj) * G;
-                    if constexpr (G == 4) {
-                        *reinterpret_cast<float4*>(dst) = make_float4(z[0], z[1], z[2], z[3]);
-                    } else {
 #pragma unroll
-                        for (int g = 0; g < G; ++g) dst[g] = z[g];
-                    }
+                    for (int g = 0; g < G; ++g) dst[g] = z[g];
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
                         if (z[g] > m[g]) {
@@ -152,41 +153,46 @@ __global__ void __launch_bounds__((kScoreWarps + 1) * 32) k_score(ScoreParams p)
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
         }
-        // merge the lanes' (max, sum) and publish this warp's record for unit u
+        // merge the lanes' (max, sum) and publish this warp's record for run r
 #pragma unroll
         for (int g = 0; g < G; ++g) {
             const float M = warp_max(m[g]);
             const float t = (m[g] == -CUDART_INF_F) ? 0.f : sx[g] * __expf(m[g] - M);
             const float S = warp_sum(t);
-            if (lane == 0)
-                p.part[((static_cast<int64_t>(blockIdx.x) * p.slots + slot) * p.nparts + warp) * G + g] =
-                    make_float2(M, S);
+            if (lane == 0) p.part[(static_cast<int64_t>(r) * kScoreWarps + warp) * G + g] = make_float2(M, S);
         }
-        pos = uend;
-        if (!ok) break;
     }
 }
 
 // ------------------------------------------------------------------ tensor-core path
+// What flows from the producer to the MMA thread (per stage) and from the MMA
+// thread to the epilogue (per accumulator buffer).
+struct ScTile {
+    int run;        // -1: no more work
+    int nv;         // valid landmarks in the tile
+    int64_t j;      // flat index of the tile's first landmark
+    int unit;
+    int last;       // last tile of its run
+};
+
 template <int G>
 __global__ void __launch_bounds__(192, 1) k_score_tc(const __grid_constant__ CUtensorMap tmL, ScoreParams p) {
+    // stage s: [2 K-blocks][128 landmark rows][128 B] then [2 K-blocks][16 query rows][128 B]
+    constexpr int kStage = 32768 + 4096;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sL = smem;                                  // kScStages x (2 x [128 rows][128 B])
-    uint8_t* sQ = smem + kScStages * 32768;              // 2 x [16 rows][128 B]
-    __shared__ uint64_t full[kScStages], empty[kScStages], accf[2], acce[2], qdone;
+    __shared__ uint64_t full[kScStages], empty[kScStages], accf[2], acce[2], drain;
+    __shared__ ScTile stile[kScStages], atile[2];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * p.per;
-    const int64_t c1 = min(c0 + p.per, p.total);
-    if (c0 >= c1) return;   // uniform
     const int64_t n_c = p.n_c;
     if (tid == 0) {
         for (int s = 0; s < kScStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-        for (int b = 0; b < 2; ++b) { mbar_init(&accf[b], 1); mbar_init(&acce[b], 4); }
-        mbar_init(&qdone, 1);
+        // accf: the MMA commit (accumulator complete) + a release-arrive after the tile record is written
+        for (int b = 0; b < 2; ++b) { mbar_init(&accf[b], 2); mbar_init(&acce[b], 4); }
+        mbar_init(&drain, 1);
         s_abort = 0;
         fence_mbar_init();
         prefetch_tensormap(&tmL);
@@ -201,140 +207,174 @@ __global__ void __launch_bounds__(192, 1) k_score_tc(const __grid_constant__ CUt
     const uint32_t tmem = tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer
-        if (lane == 0) {
-            int it = 0;
-            for (int64_t pos = c0; pos < c1 && !s_abort;) {
-                const int64_t u = pos / n_c, uend = min(c1, (u + 1) * n_c);
-                for (int64_t j = pos; j < uend; j += kScTile, ++it) {
-                    const int s = it % kScStages;
-                    if (!mbar_wait(&empty[s], ((it / kScStages) & 1) ^ 1)) {
-                        set_err(p.err, DEV_ERR_TIMEOUT, 111);
-                        s_abort = 1;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&full[s], 32768);
-                    tma_load_2d(sL + s * 32768, &tmL, 0, static_cast<int>(j), &full[s]);
-                    tma_load_2d(sL + s * 32768 + 16384, &tmL, 64, static_cast<int>(j), &full[s]);
+        // ------------------------------------------------ producer warp: claims runs, writes each
+        // stage's query tile (rows g < G; the MMA's other columns are never read) and issues the
+        // landmark copies
+        constexpr int QW = (G * 16 + 31) / 32;   // 16-byte words of the query rows per lane
+        int it = 0;
+        int next = (lane == 0) ? atomicAdd(p.sched, 1) : 0;
+        next = __shfl_sync(0xffffffffu, next, 0);
+        bool done = false;
+        while (!done) {
+            const int r = s_abort ? p.total_runs : next;
+            int64_t a = 0, e = 0;
+            int u = 0;
+            if (r < p.total_runs) {
+                u = r / p.nru;
+                a = static_cast<int64_t>(u) * n_c + static_cast<int64_t>(r % p.nru) * kRunChunks;
+                e = min(a + kRunChunks, static_cast<int64_t>(u + 1) * n_c);
+                int nx = (lane == 0) ? atomicAdd(p.sched, 1) : 0;   // claim the next run early
+                next = __shfl_sync(0xffffffffu, nx, 0);
+            } else {
+                done = true;
+            }
+            uint4 qw[QW];
+#pragma unroll
+            for (int k = 0; k < QW; ++k) {
+                const int w = lane + 32 * k, n = w >> 4, c16 = w & 15;
+                qw[k] = make_uint4(0, 0, 0, 0);
+                if (!done && n < G)
+                    qw[k] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
+                                                            (static_cast<int64_t>(u) * G + n) * kD + c16 * 8);
+            }
+            for (int64_t j = a; done || j < e; j += kScTile, ++it) {
+                const int s = it % kScStages;
+                uint8_t* st = smem + s * kStage;
+                const int okw = mbar_wait(&empty[s], ((it / kScStages) & 1) ^ 1) ? 1 : 0;
+                if (!__all_sync(0xffffffffu, okw)) {
+                    if (lane == 0) set_err(p.err, DEV_ERR_TIMEOUT, 111);
+                    s_abort = 1;
+                    done = true;
                 }
-                pos = uend;
+                if (done) {   // end marker: a plain arrival completes the stage's phase
+                    if (lane == 0) {
+                        stile[s].run = -1;
+                        mbar_arrive(&full[s]);
+                    }
+                    ++it;
+                    break;
+                }
+#pragma unroll
+                for (int k = 0; k < QW; ++k) {
+                    const int w = lane + 32 * k, n = w >> 4, c16 = w & 15, kb = c16 >> 3, c = c16 & 7;
+                    if (n < G)
+                        *reinterpret_cast<uint4*>(st + 32768 + kb * 2048 + (n >> 3) * 1024 + (n & 7) * 128 +
+                                                  ((c ^ (n & 7)) << 4)) = qw[k];
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    ScTile t;
+                    t.run = r;
+                    t.j = j;
+                    t.nv = static_cast<int>(min(static_cast<int64_t>(kScTile), e - j));
+                    t.unit = u;
+                    t.last = (j + kScTile >= e);
+                    stile[s] = t;
+                    mbar_arrive_expect_tx(&full[s], 32768);
+                    tma_load_2d(st, &tmL, 0, static_cast<int>(j), &full[s]);
+                    tma_load_2d(st + 16384, &tmL, 64, static_cast<int>(j), &full[s]);
+                }
+                __syncwarp();
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer (whole warp writes the query tile)
+        // ------------------------------------------------ MMA issuer
         constexpr uint32_t idesc = idesc_bf16_f32(kScTile, kScN);
-        int it = 0, qphase = 0;
-        bool first = true;
-        for (int64_t pos = c0; pos < c1 && !s_abort;) {
-            const int64_t u = pos / n_c, uend = min(c1, (u + 1) * n_c);
-            // the unit's queries as the B operand: rows g < G, zero rows up to 16
-            if (!first) {
-                if (lane == 0) tc_commit(&qdone);
-                __syncwarp();
-                if (!mbar_wait(&qdone, qphase & 1)) { set_err(p.err, DEV_ERR_TIMEOUT, 112); s_abort = 1; }
-                ++qphase;
+        int it = 0;
+        while (true) {
+            const int s = it % kScStages, b = it & 1;
+            int ok = mbar_wait(&full[s], (it / kScStages) & 1) ? 1 : 0;
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) { if (lane == 0) set_err(p.err, DEV_ERR_TIMEOUT, 112); s_abort = 1; break; }
+            const ScTile t = stile[s];
+            // the accumulator buffer must be free before its record is replaced
+            if (lane == 0) ok = mbar_wait(&acce[b], ((it >> 1) & 1) ^ 1) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) { if (lane == 0) set_err(p.err, DEV_ERR_TIMEOUT, 113); s_abort = 1; break; }
+            if (t.run < 0) {
+                if (lane == 0) { atile[b] = t; mbar_arrive_cnt(&accf[b], 2); }
+                break;
             }
-            first = false;
-            for (int e = lane; e < kScN * 16; e += 32) {
-                const int n = e >> 4, c16 = e & 15, kb = c16 >> 3, c = c16 & 7;
-                uint4 w = make_uint4(0, 0, 0, 0);
-                if (n < G)
-                    w = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
-                                                        (u * G + n) * kD + kb * 64 + c * 8);
-                *reinterpret_cast<uint4*>(sQ + kb * 2048 + (n >> 3) * 1024 + (n & 7) * 128 + ((c ^ (n & 7)) << 4)) = w;
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            for (int64_t j = pos; j < uend; j += kScTile, ++it) {
-                const int s = it % kScStages, b = it & 1;
-                bool ok = true;
-                if (lane == 0) {
-                    ok = mbar_wait(&full[s], (it / kScStages) & 1) && mbar_wait(&acce[b], ((it >> 1) & 1) ^ 1);
-                    if (ok) {
-                        tc_fence_after();
-                        uint32_t acc = 0;
-                        for (int kb = 0; kb < 2; ++kb)
-                            for (int k = 0; k < 4; ++k) {
-                                const uint64_t ad = smem_desc_sw128(smem_u32(sL + s * 32768 + kb * 16384 + k * 32));
-                                const uint64_t bd = smem_desc_sw128(smem_u32(sQ + kb * 2048 + k * 32));
-                                tc_mma_bf16(tmem + b * kScN, ad, bd, idesc, acc);
-                                acc = 1;
-                            }
-                        tc_commit(&empty[s]);
-                        tc_commit(&accf[b]);
-                    } else {
-                        set_err(p.err, DEV_ERR_TIMEOUT, 113);
-                        s_abort = 1;
+            if (lane == 0) {
+                tc_fence_after();
+                const uint8_t* st = smem + s * kStage;
+                uint32_t acc = 0;
+                for (int kb = 0; kb < 2; ++kb)
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t ad = smem_desc_sw128(smem_u32(st + kb * 16384 + k * 32));
+                        const uint64_t bd = smem_desc_sw128(smem_u32(st + 32768 + kb * 2048 + k * 32));
+                        tc_mma_bf16(tmem + b * kScN, ad, bd, idesc, acc);
+                        acc = 1;
                     }
-                }
-                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0);
-                if (!ok) break;
+                tc_commit(&empty[s]);
+                tc_commit(&accf[b]);
+                atile[b] = t;
+                mbar_arrive(&accf[b]);   // release: the record is visible once the phase completes
             }
-            pos = uend;
+            __syncwarp();
+            ++it;
         }
         // every MMA retired before the accumulator is released
-        if (lane == 0) tc_commit(&qdone);
+        if (lane == 0) tc_commit(&drain);
         __syncwarp();
-        (void)mbar_wait(&qdone, qphase & 1);
+        (void)mbar_wait(&drain, 0);
     } else {
         // ------------------------------------------------ epilogue: 4 warps, one landmark row per thread
         const int quarter = warp & 3;                     // TMEM lanes [32*quarter, +32)
         const int row = quarter * 32 + lane;
         const int ew = warp - 2;
-        int it = 0, slot = 0;
-        for (int64_t pos = c0; pos < c1; ++slot) {
-            const int64_t u = pos / n_c, uend = min(c1, (u + 1) * n_c);
-            float m[G], sx[G];
+        float m[G], sx[G];
 #pragma unroll
-            for (int g = 0; g < G; ++g) { m[g] = -CUDART_INF_F; sx[g] = 0.f; }
-            for (int64_t j = pos; j < uend && !s_abort; j += kScTile, ++it) {
-                const int b = it & 1;
-                const int nv = static_cast<int>(min(static_cast<int64_t>(kScTile), uend - j));
-                if (!mbar_wait(&accf[b], (it >> 1) & 1)) {
-                    set_err(p.err, DEV_ERR_TIMEOUT, 114);
-                    s_abort = 1;
-                    break;
+        for (int g = 0; g < G; ++g) { m[g] = -CUDART_INF_F; sx[g] = 0.f; }
+        for (int it = 0;; ++it) {
+            const int b = it & 1;
+            if (!mbar_wait(&accf[b], (it >> 1) & 1)) {
+                set_err(p.err, DEV_ERR_TIMEOUT, 115);
+                s_abort = 1;
+                break;
+            }
+            const ScTile t = atile[b];
+            if (t.run < 0) break;
+            tc_fence_after();
+            float v[8];
+            tmem_ld8(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + b * kScN, v);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acce[b]);
+            if (row < t.nv) {
+                float z[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) z[g] = v[g] * p.scale;
+                float* dst = p.logits + (t.j + row) * G;
+                if constexpr (G == 4) {
+                    *reinterpret_cast<float4*>(dst) = make_float4(z[0], z[1], z[2], z[3]);
+                } else {
+#pragma unroll
+                    for (int g = 0; g < G; ++g) dst[g] = z[g];
                 }
-                tc_fence_after();
-                float v[8];
-                tmem_ld8(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + b * kScN, v);
-                tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&acce[b]);
-                if (row < nv) {
-                    float z[G];
 #pragma unroll
-                    for (int g = 0; g < G; ++g) z[g] = v[g] * p.scale;
-                    float* dst = p.logits + (j + row) * G;
-                    if constexpr (G == 4) {
-                        *reinterpret_cast<float4*>(dst) = make_float4(z[0], z[1], z[2], z[3]);
+                for (int g = 0; g < G; ++g) {
+                    if (z[g] > m[g]) {
+                        sx[g] = sx[g] * __expf(m[g] - z[g]) + 1.f;
+                        m[g] = z[g];
                     } else {
-#pragma unroll
-                        for (int g = 0; g < G; ++g) dst[g] = z[g];
-                    }
-#pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        if (z[g] > m[g]) {
-                            sx[g] = sx[g] * __expf(m[g] - z[g]) + 1.f;
-                            m[g] = z[g];
-                        } else {
-                            sx[g] += __expf(z[g] - m[g]);
-                        }
+                        sx[g] += __expf(z[g] - m[g]);
                     }
                 }
             }
+            if (t.last) {
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float M = warp_max(m[g]);
-                const float t = (m[g] == -CUDART_INF_F) ? 0.f : sx[g] * __expf(m[g] - M);
-                const float S = warp_sum(t);
-                if (lane == 0)
-                    p.part[((static_cast<int64_t>(blockIdx.x) * p.slots + slot) * kScParts + ew) * G + g] =
-                        make_float2(M, S);
+                for (int g = 0; g < G; ++g) {
+                    const float M = warp_max(m[g]);
+                    const float tt = (m[g] == -CUDART_INF_F) ? 0.f : sx[g] * __expf(m[g] - M);
+                    const float S = warp_sum(tt);
+                    if (lane == 0) p.part[(static_cast<int64_t>(t.run) * kScParts + ew) * G + g] = make_float2(M, S);
+                    m[g] = -CUDART_INF_F;
+                    sx[g] = 0.f;
+                }
             }
-            pos = uend;
-            if (s_abort) break;
         }
     }
     tc_fence_before();
@@ -347,7 +387,7 @@ __global__ void __launch_bounds__(192, 1) k_score_tc(const __grid_constant__ CUt
 
 template <int G>
 static int launch_tc(const CUtensorMap* tmL, const ScoreParams& p, int ncta, cudaStream_t s) {
-    const int smem = kScStages * 32768 + 2 * 2048 + 1024;
+    const int smem = kScStages * (32768 + 4096) + 1024;
     cudaFuncSetAttribute(k_score_tc<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     k_score_tc<G><<<ncta, 192, smem, s>>>(*tmL, p);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
@@ -398,7 +438,7 @@ int score_parts(int dtype) { return dtype == 1 ? kScParts : kScoreWarps; }
 int score_ctas_per_sm(int dtype, int G) {
     if (dtype == 1) {
         (void)G;
-        return 1;   // the tensor-core kernel holds 133 KB of shared memory
+        return 1;   // the tensor-core kernel holds 217 KB of shared memory
     } else {
 #define OCCF(g) occ_t<float, g>()
         SKV_G_DISPATCH(G, OCCF)

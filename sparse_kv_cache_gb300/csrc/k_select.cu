@@ -291,33 +291,23 @@ __global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
         }
     }
 
-    // 1. log-sum-exp of every query head from the scoring partials
+    // 1. log-sum-exp of every query head from the scoring runs' records
     if (warp < G) {
-        const int64_t c_first = (static_cast<int64_t>(u) * n) / p.per;
-        const int64_t c_last = (static_cast<int64_t>(u + 1) * n - 1) / p.per;
         const int np = p.nparts;
-        const int64_t nrec = (c_last - c_first + 1) * np;
+        const int nrec = p.nru * np;
+        const float2* rec = p.part + static_cast<int64_t>(u) * nrec * G;
         float M = -CUDART_INF_F;
-        for (int64_t r = lane; r < nrec; r += 32) {
-            const int64_t c = c_first + r / np;
-            const int w = static_cast<int>(r % np);
-            const int slot = static_cast<int>(u - (c * p.per) / n);
-            if (c >= p.ncta || slot < 0 || slot >= p.slots) { set_err(p.err, DEV_ERR_BOUNDS, 311); continue; }
-            M = fmaxf(M, p.part[((c * p.slots + slot) * np + w) * G + warp].x);
-        }
+        for (int r = lane; r < nrec; r += 32) M = fmaxf(M, rec[r * G + warp].x);
         M = warp_max(M);
         float S = 0.f;
-        for (int64_t r = lane; r < nrec; r += 32) {
-            const int64_t c = c_first + r / np;
-            const int w = static_cast<int>(r % np);
-            const int slot = static_cast<int>(u - (c * p.per) / n);
-            if (c >= p.ncta || slot < 0 || slot >= p.slots) continue;
-            const float2 ms = p.part[((c * p.slots + slot) * np + w) * G + warp];
+        for (int r = lane; r < nrec; r += 32) {
+            const float2 ms = rec[r * G + warp];
             if (ms.x != -CUDART_INF_F) S += ms.y * __expf(ms.x - M);
         }
         S = warp_sum(S);
         if (lane == 0) sh.lse[warp] = M + __logf(S);
     }
+    if (u == 0 && tid == 0 && p.sched) *p.sched = 0;   // the scoring kernel of this step is done
     __syncthreads();
     // 2. v_j = max_g (z_gj - lse_g)
     float lse[G];

@@ -26,16 +26,18 @@ constexpr int kScStages = 6;
 constexpr int kScN = 16;          // MMA N: the G <= 8 query heads, zero-padded
 constexpr int kScParts = 4;       // partial records per (CTA, unit): one per epilogue warp
 
+constexpr int kRunChunks = 512;   // landmarks per unit of scheduled scoring work
+
 struct ScoreParams {
     const void* L;        // [U][n_c][d]
     const void* q;        // [U*G][d]
     float* logits;        // [U][n_c][G]  z = q.L / sqrt(d)
-    float2* part;         // [ncta][slots][nparts][G] (max, sum exp(z - max))
+    float2* part;         // [U * nru][nparts][G] (max, sum exp(z - max)) per run
     int n_c;
-    int64_t total;        // U * n_c
-    int64_t per;          // chunks per CTA
-    int slots;            // max units one CTA touches
-    int nparts;           // partial records per (CTA, unit)
+    int nru;              // runs per unit: ceil(n_c / kRunChunks)
+    int total_runs;       // U * nru
+    int nparts;           // records per run
+    int* sched;           // run counter (reset to 0 by the selection kernel)
     float scale;
     int* err;
 };
@@ -52,7 +54,8 @@ struct SelectParams {
     int U, H, G;
     // decode: scores from logits and score partials
     const float* logits; const float2* part;
-    int64_t per; int slots; int ncta; int nparts;
+    int nru; int nparts;
+    int* sched;           // scoring run counter, reset here for the next step
     // outlier mode: score = -src[u][j]
     const float* neg_src;
     float* vbuf;          // [U][n] global score buffer when n exceeds shared memory
@@ -111,7 +114,6 @@ struct GatherParams {
     int* err;
 };
 int launch_gather(const GatherParams& p, int grid_x, cudaStream_t s);
-int launch_fetch(const GatherParams& p, int grid, cudaStream_t s);   // bf16 decode misses
 
 struct CompactParams {
     const float* Lfull; int64_t ncand;   // [U][ncand][d]

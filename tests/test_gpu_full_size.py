@@ -15,7 +15,7 @@ def test_llama_32k_b4():
 
 def test_llama_128k_b8_host_values():
     rep = run_and_check(LLAMA_128K, 4, units=[0, 37, 63], gen_device="cuda", check_cache=False,
-                        host_alloc="huge")
+                        host_alloc="arena")
     assert rep.steps == 4
 
 

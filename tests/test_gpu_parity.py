@@ -39,9 +39,9 @@ def test_bf16_host_pinned_values():
     run_and_check(SMALL_BF16.with_(v_place="host", seed=12), 5)
 
 
-def test_bf16_host_huge_page_values():
-    # system memory from shadowkv_host_alloc, read by the GPU through the host page tables
-    run_and_check(SMALL_BF16.with_(v_place="host", seed=14), 4, host_alloc="huge")
+def test_bf16_host_arena_values():
+    # page-locked memory from shadowkv_host_alloc, passed as an interior slice
+    run_and_check(SMALL_BF16.with_(v_place="host", seed=14), 4, host_alloc="arena")
 
 
 def test_full_budget_selects_every_chunk():
