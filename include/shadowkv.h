@@ -223,6 +223,56 @@ int shadowkv_model(const skv_config* cfg, double alpha, int64_t t, double b_gpu_
 int shadowkv_host_alloc(size_t bytes, void** out);
 void shadowkv_host_free(void* p);
 
+/*
+ * Sparse attention that allocates nothing.  The pages have no counterpart to
+ * this call; it exists for callers that cannot allocate device memory while
+ * they run -- a server that hands all of HBM to one pool at start-up, code
+ * that runs under an allocator lock, or a hot path where an allocation (which
+ * may synchronise the device) is forbidden.
+ *
+ * It computes what step 5 of shadowkv_decode_step computes, with the same
+ * kernel: for each unit u (a batch element's KV head) and each of its G query
+ * heads, out = softmax(q.K^T / sqrt(d)).V over the unit's outlier rows, then
+ * its cache rows, then its first n_local_tokens local rows, all bf16, d = 128,
+ * rows of a region contiguous per unit:
+ *   q         dev [units*group][128]                    (post-RoPE)
+ *   k/v_outlier dev [units][n_outlier_tokens][128]      (may be NULL if 0 rows)
+ *   k/v_cache dev [units][n_cache_tokens][128]          (may be NULL if 0 rows)
+ *   k/v_local dev [units][local_capacity][128]
+ *   out       dev [units*group][128]                    written
+ * The caller owns every buffer.  The kernel's scratch (partial results of the
+ * 128-token splits and one merge ticket per unit) lives in a fixed 16 MiB
+ * array compiled into the library, which every GPU that loads the library
+ * holds until the process exits.  A shape whose scratch does not fit --
+ * units * ceil(rows / 128) * group * 528 bytes above 16 MiB - 64 KiB, or more
+ * than 16384 units -- is rejected with SKV_ERR_INVALID; fp32 data with
+ * SKV_ERR_UNSUPPORTED.  No cudaMalloc, cudaFree or other allocating call is
+ * made.  The first call on a device resolves the array's device address for
+ * that device (it must be the current device), so make that first call before
+ * any stream capture.  Every call shares the one array and clears the merge
+ * tickets itself (asynchronously, on `stream`); calls that overlap on the GPU
+ * -- on different streams, or from different threads -- race on it, so
+ * serialise them.
+ */
+typedef struct {
+    int32_t units;              /* b*H */
+    int32_t group;              /* G in {1, 2, 4, 8} */
+    int32_t dtype;              /* skv_dtype; only SKV_BF16 */
+    int32_t n_outlier_tokens;   /* rows per unit in k/v_outlier */
+    int32_t n_cache_tokens;     /* rows per unit in k/v_cache */
+    int32_t n_local_tokens;     /* rows per unit used from k/v_local, >= 1 */
+    int32_t local_capacity;     /* rows per unit allocated in k/v_local */
+    const void* q;
+    const void* k_outlier;
+    const void* v_outlier;
+    const void* k_cache;
+    const void* v_cache;
+    const void* k_local;
+    const void* v_local;
+    void* out;
+} skv_attention_args;
+int shadowkv_sparse_attention_noalloc(const skv_attention_args* args, skv_stream stream);
+
 void shadowkv_destroy(skv_layer* layer);   /* frees everything the handle owns; NULL ok */
 const char* shadowkv_strerror(int code);
 int shadowkv_version(void);                 /* major*10000 + minor*100 + patch */

@@ -4,5 +4,6 @@ The compute path is libshadowkv.so (hand-written CUDA kernels behind the C
 ABI in include/shadowkv.h); this package is its ctypes binding.
 """
 from ._binding import (FIELDS, PHASES, SKV_BF16, SKV_F32, SKV_V_HBM, SKV_V_HOST,  # noqa: F401
-                       HostBuffer, Layer, ShadowKVError, SkvConfig, load, make_config, model, strerror,
+                       HostBuffer, Layer, ShadowKVError, SkvConfig, load, make_config, model,
+                       sparse_attention_noalloc, strerror,
                        validate_config)

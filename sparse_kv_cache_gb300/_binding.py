@@ -25,7 +25,8 @@ ERRORS = {0: "OK", -1: "INVALID", -2: "OOM", -3: "NOT_PINNED", -4: "CUDA", -5: "
 EXPORTED = ("shadowkv_validate_config", "shadowkv_prefill_index", "shadowkv_decode_step",
             "shadowkv_stats", "shadowkv_reset_stats", "shadowkv_set_profiling",
             "shadowkv_export_size", "shadowkv_export", "shadowkv_model", "shadowkv_destroy",
-            "shadowkv_strerror", "shadowkv_version", "shadowkv_host_alloc", "shadowkv_host_free")
+            "shadowkv_strerror", "shadowkv_version", "shadowkv_host_alloc", "shadowkv_host_free",
+            "shadowkv_sparse_attention_noalloc")
 
 
 class SkvConfig(ctypes.Structure):
@@ -46,6 +47,15 @@ class SkvStats(ctypes.Structure):
                 ("scratch_bytes", ctypes.c_double),
                 ("phase_ms", ctypes.c_double * 5), ("phase_launches", ctypes.c_int64 * 5),
                 ("device_error", ctypes.c_int32)]
+
+
+class SkvAttentionArgs(ctypes.Structure):
+    _fields_ = [("units", ctypes.c_int32), ("group", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("n_outlier_tokens", ctypes.c_int32), ("n_cache_tokens", ctypes.c_int32),
+                ("n_local_tokens", ctypes.c_int32), ("local_capacity", ctypes.c_int32),
+                ("q", ctypes.c_void_p), ("k_outlier", ctypes.c_void_p), ("v_outlier", ctypes.c_void_p),
+                ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p), ("k_local", ctypes.c_void_p),
+                ("v_local", ctypes.c_void_p), ("out", ctypes.c_void_p)]
 
 
 class SkvModel(ctypes.Structure):
@@ -93,6 +103,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.shadowkv_host_alloc.restype = i32
     lib.shadowkv_host_free.argtypes = [vp]
     lib.shadowkv_host_free.restype = None
+    lib.shadowkv_sparse_attention_noalloc.argtypes = [ctypes.POINTER(SkvAttentionArgs), vp]
+    lib.shadowkv_sparse_attention_noalloc.restype = i32
     for name in ("shadowkv_validate_config", "shadowkv_prefill_index", "shadowkv_decode_step",
                  "shadowkv_stats", "shadowkv_reset_stats", "shadowkv_set_profiling",
                  "shadowkv_export", "shadowkv_model", "shadowkv_version"):
@@ -133,6 +145,18 @@ def model(cfg: SkvConfig, alpha: float, t: int, b_gpu_gbs: float, b_link_gbs: fl
     _check(load().shadowkv_model(ctypes.byref(cfg), alpha, t, b_gpu_gbs, b_link_gbs, ctypes.byref(out)),
            "shadowkv_model")
     return {k: getattr(out, k) for k, _ in SkvModel._fields_}
+
+
+def sparse_attention_noalloc(q, k_outlier, v_outlier, k_cache, v_cache, k_local, v_local, out,
+                             units: int, group: int, n_outlier_tokens: int, n_cache_tokens: int,
+                             n_local_tokens: int, local_capacity: int, stream=None) -> int:
+    """shadowkv_sparse_attention_noalloc (bf16 tensors); returns the status code."""
+    a = SkvAttentionArgs(units=units, group=group, dtype=SKV_BF16, n_outlier_tokens=n_outlier_tokens,
+                         n_cache_tokens=n_cache_tokens, n_local_tokens=n_local_tokens,
+                         local_capacity=local_capacity, q=_ptr(q), k_outlier=_ptr(k_outlier),
+                         v_outlier=_ptr(v_outlier), k_cache=_ptr(k_cache), v_cache=_ptr(v_cache),
+                         k_local=_ptr(k_local), v_local=_ptr(v_local), out=_ptr(out))
+    return load().shadowkv_sparse_attention_noalloc(ctypes.byref(a), _stream(stream))
 
 
 def _ptr(t) -> int | None:

@@ -15,6 +15,10 @@
 // fp32 and writes the output row.  Each key and value byte is read once.
 #include <math_constants.h>
 
+#include <cmath>
+#include <mutex>
+
+#include "shadowkv.h"
 #include "skv_common.cuh"
 #include "skv_internal.h"
 
@@ -410,3 +414,90 @@ int launch_attn(int dtype, const AttnParams& p, cudaStream_t s) {
 }
 
 }  // namespace skv
+
+// ---------------------------------------------------------------------------
+// Sparse attention without any allocation.
+//
+// Some callers cannot allocate device memory while they run: an inference
+// server that carves every byte of HBM out of one pool at start-up, code that
+// runs under an allocator lock, or an integration that forbids cudaMalloc on
+// its hot path because an allocation may synchronise the device.  This entry
+// point serves them: it runs the same split-K attention kernel as the decode
+// step over key/value regions the caller provides, and keeps the kernel's
+// scratch -- the per-split partial results and the per-unit merge tickets --
+// in one fixed array compiled into this library instead of memory allocated
+// for a layer.  It calls no cudaMalloc, cudaFree or other allocating routine.
+namespace skv {
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;   // whole array: 16 MiB
+constexpr size_t kNoAllocTicketBytes = size_t(64) << 10;    // merge tickets of up to 16384 units
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+static std::mutex g_noalloc_mu;
+static void* g_noalloc_addr[256];   // per device: the array's device address, once resolved
+
+template <int G>
+static int launch_bulk_with(const AttnParams& p, cudaStream_t s) { return launch_bulk<G>(p, s); }
+}  // namespace skv
+
+extern "C" int shadowkv_sparse_attention_noalloc(const skv_attention_args* a, skv_stream stream) {
+    using namespace skv;
+    if (!a) return SKV_ERR_INVALID;
+    if (a->dtype != SKV_BF16) return SKV_ERR_UNSUPPORTED;
+    const int G = a->group;
+    if (a->units < 1 || (G != 1 && G != 2 && G != 4 && G != 8)) return SKV_ERR_INVALID;
+    if (a->n_outlier_tokens < 0 || a->n_cache_tokens < 0 || a->n_local_tokens < 1 ||
+        a->n_local_tokens > a->local_capacity)
+        return SKV_ERR_INVALID;
+    const void* ptrs[] = {a->q, a->k_outlier, a->v_outlier, a->k_cache, a->v_cache, a->k_local, a->v_local, a->out};
+    for (const void* p : ptrs)
+        if (reinterpret_cast<uintptr_t>(p) & 15) return SKV_ERR_INVALID;
+    if (!a->q || !a->k_local || !a->v_local || !a->out) return SKV_ERR_INVALID;
+    if ((a->n_outlier_tokens && (!a->k_outlier || !a->v_outlier)) || (a->n_cache_tokens && (!a->k_cache || !a->v_cache)))
+        return SKV_ERR_INVALID;
+    const int64_t ntot = static_cast<int64_t>(a->n_outlier_tokens) + a->n_cache_tokens + a->n_local_tokens;
+    const int64_t nsplit = (ntot + kBSeg - 1) / kBSeg;
+    const int64_t part_bytes = static_cast<int64_t>(a->units) * nsplit * G * kPartPitch * 4;
+    if (nsplit > (1 << 20) || static_cast<int64_t>(a->units) * 4 > static_cast<int64_t>(kNoAllocTicketBytes) ||
+        part_bytes > static_cast<int64_t>(kNoAllocScratchBytes - kNoAllocTicketBytes))
+        return SKV_ERR_INVALID;   // the shape needs more scratch than the fixed array holds
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return SKV_ERR_CUDA;
+    void* base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        if (!g_noalloc_addr[dev]) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+                cudaGetLastError();
+                return SKV_ERR_CUDA;
+            }
+            g_noalloc_addr[dev] = p;
+        }
+        base = g_noalloc_addr[dev];
+    }
+    // the merge tickets must start at zero; the partials are fully overwritten
+    if (cudaMemsetAsync(base, 0, static_cast<size_t>(a->units) * 4, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SKV_ERR_CUDA;
+    }
+    AttnParams p{};
+    p.q = a->q;
+    p.k_out = a->k_outlier; p.v_out = a->v_outlier; p.n_out = a->n_outlier_tokens;
+    p.k_c = a->k_cache; p.v_c = a->v_cache; p.n_cache = a->n_cache_tokens;
+    p.k_loc = a->k_local; p.v_loc = a->v_local; p.n_loc = a->n_local_tokens; p.loc_cap = a->local_capacity;
+    p.out = a->out;
+    p.counter = static_cast<int*>(base);
+    p.part = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + kNoAllocTicketBytes);
+    p.nsplit = static_cast<int>(nsplit);
+    p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(kD)));
+    p.G = G; p.U = a->units; p.err = nullptr;
+    int rc = -1;
+    switch (G) {
+        case 1: rc = launch_bulk_with<1>(p, stream); break;
+        case 2: rc = launch_bulk_with<2>(p, stream); break;
+        case 4: rc = launch_bulk_with<4>(p, stream); break;
+        case 8: rc = launch_bulk_with<8>(p, stream); break;
+    }
+    return rc == 0 ? SKV_OK : SKV_ERR_CUDA;
+}

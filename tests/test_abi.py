@@ -58,8 +58,8 @@ def test_struct_layouts_match_header(lib):
     if gcc is None:
         pytest.skip("gcc missing")
     prog = ('#include "shadowkv.h"\n#include <stdio.h>\n#include <stddef.h>\n'
-            'int main(){printf("%zu %zu %zu %zu\\n", sizeof(skv_config), sizeof(skv_stats), '
-            'sizeof(skv_model), offsetof(skv_stats, device_error));return 0;}\n')
+            'int main(){printf("%zu %zu %zu %zu %zu\\n", sizeof(skv_config), sizeof(skv_stats), '
+            'sizeof(skv_model), offsetof(skv_stats, device_error), sizeof(skv_attention_args));return 0;}\n')
     tmp = os.path.join(ROOT, "sparse_kv_cache_gb300", "_build")
     os.makedirs(tmp, exist_ok=True)
     c = os.path.join(tmp, "abi_sizes.c")
@@ -68,7 +68,7 @@ def test_struct_layouts_match_header(lib):
     subprocess.run([gcc, "-I", os.path.dirname(src), c, "-o", exe], check=True)
     sizes = [int(x) for x in subprocess.run([exe], capture_output=True, text=True).stdout.split()]
     assert sizes == [ctypes.sizeof(lib.SkvConfig), ctypes.sizeof(lib.SkvStats), ctypes.sizeof(lib.SkvModel),
-                     lib.SkvStats.device_error.offset]
+                     lib.SkvStats.device_error.offset, ctypes.sizeof(lib.SkvAttentionArgs)]
 
 
 def test_strerror_and_version(lib):
