@@ -29,6 +29,12 @@ sys.path.insert(0, ROOT)
 
 from workload import ALL, LLAMA_128K, Workload  # noqa: E402
 
+# DRAM traffic of one k_score_tc launch from an ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum = 133.89 + 6.17 MB over 32 units at 128K, bf16), valid only while
+# the scorer source is the one that was profiled; per unit, scaled to a launch by its units.
+SCORE_TRAFFIC = {"source_sha256": "e563c2bad4e955c6434ffcaa4b44fa88fafd83a7f9791fe79bc084448f3a5167",
+                 "seq_len": 131072, "dtype": "bf16", "bytes_per_unit": (133885440 + 6167040) / 32}
+
 METRIC = "sparse decode-attention tokens/s and HBM GB/s (% of 8 TB/s) at 128K, 1×GB300"
 UNIT = "tokens/s"
 
@@ -72,6 +78,34 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def max_over_ranks(x: float, ws: int, device=None) -> float:
+    """The maximum of a per-rank value over all ranks (identity on one rank)."""
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_seed(base: int, rank: int) -> int:
+    """Each rank runs its own independent replica of the workload."""
+    return base + 1000 * rank
+
+
+def score_traffic_per_launch(w: Workload):
+    """Measured DRAM bytes per scorer launch, or None once the scorer or the shape differ."""
+    import hashlib
+    src = os.path.join(ROOT, "sparse_kv_cache_gb300", "csrc", "k_score.cu")
+    with open(src, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()
+    t = SCORE_TRAFFIC
+    if digest != t["source_sha256"] or w.seq_len != t["seq_len"] or w.dtype != t["dtype"]:
+        return None
+    return t["bytes_per_unit"] * w.units
 
 
 def measured_peaks():
@@ -155,7 +189,7 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
     K, W = args.steps, args.warmup
     passes = 3
     total_steps = W + passes * K
-    w = w.with_(seed=w.seed + 1000 * rank, steps=total_steps)
+    w = w.with_(seed=replica_seed(w.seed, rank), steps=total_steps)
     L = w.layers
     dt = storage_dtype(w)
     es = 2 if w.dtype == "bf16" else 4
@@ -216,13 +250,6 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
             dist.barrier()
         torch.cuda.synchronize()
 
-    def max_over_ranks(x: float) -> float:
-        if ws == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
     s_idx = 0
     for _ in range(W):
         step(s_idx); s_idx += 1
@@ -240,7 +267,7 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
     e1.record(main)
     barrier()
     clk = clocks.stop()
-    ms = max_over_ranks(e0.elapsed_time(e1))
+    ms = max_over_ranks(e0.elapsed_time(e1), ws, dev)
     st = [lay.stats() for lay in layers]
     hbm = sum(s["hbm_bytes"] for s in st)
     link = sum(s["link_bytes"] for s in st)
@@ -263,6 +290,7 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
     score_us = 1000.0 * phase_ms["score"] / max(1, phase_n["score"])
     score_bytes = w.units * (w.n_selectable + w.group) * w.head_dim * es   # landmarks + queries
     achieved = score_bytes / (score_us * 1e-6) / 1e9
+    score_traffic = score_traffic_per_launch(w)
     peak, peak_kind = measured_peaks()
 
     # ---- pass 3: end to end through the public call with host buffers
@@ -289,12 +317,39 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
                     oh[k, ell].copy_(out[ell], non_blocking=True)
             f1.record(main)
         barrier()
-        ms_e2e = max_over_ranks(f0.elapsed_time(f1))
+        ms_e2e = max_over_ranks(f0.elapsed_time(f1), ws, dev)
         h2d = L * (qd[0].numel() + kd[0].numel() + vd[0].numel()) * es
         d2h = L * out[0].numel() * es
         e2e = {"value": ws * w.batch * K / (ms_e2e / 1000.0), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
         s_idx += K
+
+    # host-link bandwidth, measured live: page-locked host -> HBM copy of 256 MB from the value arena
+    b_link = None
+    if arena is not None:
+        n = min(arena.tensor.numel(), (256 << 20) // es)
+        dbuf = torch.empty(n, dtype=dt, device=dev)
+        src = arena.tensor.view(-1)[:n]
+        dbuf.copy_(src, non_blocking=True)
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record()
+        for _ in range(3):
+            dbuf.copy_(src, non_blocking=True)
+        c1.record()
+        torch.cuda.synchronize()
+        b_link = 3 * n * es / (c0.elapsed_time(c1) * 1e-3) / 1e9
+        del dbuf
+    # the pages' equivalent-bandwidth model with the measured hit rate and bandwidths: predicted step time
+    peak_gbs, _ = measured_peaks()
+    cfg_m = skv.make_config(w, max_new_tokens=total_steps)
+    t_mid = W + K // 2
+    mdl = skv.model(cfg_m, max(0.0, min(1.0, alpha)), t_mid, peak_gbs, b_link or peak_gbs)
+    t_pred_ms = L * mdl["t_pred_us"] / 1000.0
+    eqbw = {"alpha_measured": alpha, "b_gpu_gbs": peak_gbs, "b_link_gbs": b_link or peak_gbs,
+            "b_link_kind": "page-locked host to HBM copy, measured" if b_link else "values in HBM",
+            "eq_bandwidth_gbs": mdl["eq_bandwidth_gbs"], "t_pred_ms_per_step": t_pred_ms,
+            "t_meas_ms_per_step": ms / K, "meas_over_pred": (ms / K) / t_pred_ms}
 
     st_all = [lay.stats(check=False) for lay in layers]
     dev_err = [s["device_error"] for s in st_all if s["device_error"]]
@@ -327,9 +382,10 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
         "alpha_mean": alpha,
         "roofline": {"bound": "hbm", "kernel": "k_score (landmark scoring)", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_kind": peak_kind, "traffic": None,
+                     "peak_kind": peak_kind, "traffic": score_traffic,
                      "algorithmic_bytes_per_launch": score_bytes, "avg_launch_us": score_us},
         "phase_ms_per_step": {ph: phase_ms[ph] / K for ph in skv.PHASES},
+        "eq_bandwidth_check": eqbw,
         "clocks": clk,
         "e2e": e2e,
         "gpu_launches": 5 * L * K,
