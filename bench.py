@@ -54,6 +54,8 @@ def parse():
                     help="reuse one layer's A/B/V for every layer (state stays per layer)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--microbatches", type=int, default=1,
+                    help="split the batch into this many handles per layer, each on its own stream pair")
     ap.add_argument("--single-stream", action="store_true",
                     help="run the value fetch on the main stream too (per-kernel timing without overlap)")
     return ap.parse_args()
@@ -199,13 +201,19 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
         share = mem_available_gb() < 1.3 * L * v_bytes / 1e9 + 16
     n_data = 1 if share else L
 
+    M = max(1, args.microbatches)
+    if w.batch % M:
+        raise SystemExit(f"batch {w.batch} is not a multiple of --microbatches {M}")
+    bm = w.batch // M
     arena = None
     if w.v_place == "host":
         # one page-locked arena for every layer's values (large allocations keep GPU translations few)
         per = w.batch * w.n_kv_heads * w.seq_len * w.head_dim
         arena = skv.HostBuffer((n_data * per,), dt)
-    main = torch.cuda.Stream(dev)
-    side = torch.cuda.Stream(dev, priority=-10)   # the value fetch (link-bound) goes first
+    # one (main, side) stream pair per micro-batch; the value fetch (link-bound) goes first
+    mains = [torch.cuda.Stream(dev) for _ in range(M)]
+    sides = [torch.cuda.Stream(dev, priority=-10) for _ in range(M)]
+    main = mains[0]
     data, layers = [], []
     t0 = time.time()
     for ell in range(n_data):
@@ -220,10 +228,13 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
         else:
             V = Vd
         data.append((A, B, V))
-    cfg = skv.make_config(w, max_new_tokens=total_steps)
+    # micro-batch m owns batch rows [m*bm, (m+1)*bm) of every tensor (all are batch-major)
+    cfg = skv.make_config(w.with_(batch=bm), max_new_tokens=total_steps)
     for ell in range(L):
         A, B, V = data[ell % n_data]
-        layers.append(skv.Layer(cfg, A, B, V, stream=main))
+        for m in range(M):
+            rows = slice(m * bm, (m + 1) * bm)
+            layers.append(skv.Layer(cfg, A[rows], B[rows], V[rows], stream=main))
     torch.cuda.synchronize()
     setup_s = time.time() - t0
 
@@ -235,14 +246,29 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
     out = [torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=dt, device=dev) for _ in range(L)]
     hq = [lay.handle for lay in layers]
     lib = skv.load()
-    ms_, ss_ = main.cuda_stream, (None if args.single_stream else side.cuda_stream)
+    ms_ = [st.cuda_stream for st in mains]
+    ss_ = [None if args.single_stream else st.cuda_stream for st in sides]
 
     def step(s: int):
+        # layer order is kept within each micro-batch's stream; the micro-batches run side by side
         for ell in range(L):
-            rc = lib.shadowkv_decode_step(hq[ell], qs[ell][s].data_ptr(), kns[ell][s].data_ptr(),
-                                          vns[ell][s].data_ptr(), out[ell].data_ptr(), None, ms_, ss_)
-            if rc:
-                raise skv.ShadowKVError(rc, "decode_step")
+            for m in range(M):
+                rows = slice(m * bm, (m + 1) * bm)
+                rc = lib.shadowkv_decode_step(hq[ell * M + m], qs[ell][s][rows].data_ptr(),
+                                              kns[ell][s][rows].data_ptr(), vns[ell][s][rows].data_ptr(),
+                                              out[ell][rows].data_ptr(), None, ms_[m], ss_[m])
+                if rc:
+                    raise skv.ShadowKVError(rc, "decode_step")
+
+    def fork(ev):
+        for st in mains[1:]:
+            st.wait_event(ev)
+
+    def join():
+        for st in mains[1:]:
+            ev = torch.cuda.Event()
+            ev.record(st)
+            main.wait_event(ev)
 
     def barrier():
         torch.cuda.synchronize()
@@ -262,8 +288,10 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(main)
+    fork(e0)
     for _ in range(K):
         step(s_idx); s_idx += 1
+    join()
     e1.record(main)
     barrier()
     clk = clocks.stop()
@@ -288,9 +316,10 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
     phase_ms = {ph: sum(s["phase_ms"][ph] for s in st2) for ph in skv.PHASES}
     phase_n = {ph: sum(s["phase_launches"][ph] for s in st2) for ph in skv.PHASES}
     score_us = 1000.0 * phase_ms["score"] / max(1, phase_n["score"])
-    score_bytes = w.units * (w.n_selectable + w.group) * w.head_dim * es   # landmarks + queries
+    # one scorer launch covers one micro-batch: landmarks + queries of its units
+    score_bytes = (w.units // M) * (w.n_selectable + w.group) * w.head_dim * es
     achieved = score_bytes / (score_us * 1e-6) / 1e9
-    score_traffic = score_traffic_per_launch(w)
+    score_traffic = score_traffic_per_launch(w.with_(batch=bm))
     peak, peak_kind = measured_peaks()
 
     # ---- pass 3: end to end through the public call with host buffers
@@ -305,17 +334,22 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
         vd = [torch.empty_like(vns[ell][0]) for ell in range(L)]
         barrier()
         f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(main):
-            f0.record(main)
-            for k in range(K):
-                for ell in range(L):
-                    qd[ell].copy_(qh[ell][k], non_blocking=True)
-                    kd[ell].copy_(kh[ell][k], non_blocking=True)
-                    vd[ell].copy_(vh[ell][k], non_blocking=True)
-                    layers[ell].decode_step(qd[ell], kd[ell], vd[ell], out[ell], None, main=main,
-                                            side=None if args.single_stream else side)
-                    oh[k, ell].copy_(out[ell], non_blocking=True)
-            f1.record(main)
+        f0.record(main)
+        fork(f0)
+        for k in range(K):
+            for ell in range(L):
+                for m in range(M):
+                    rows = slice(m * bm, (m + 1) * bm)
+                    with torch.cuda.stream(mains[m]):
+                        qd[ell][rows].copy_(qh[ell][k][rows], non_blocking=True)
+                        kd[ell][rows].copy_(kh[ell][k][rows], non_blocking=True)
+                        vd[ell][rows].copy_(vh[ell][k][rows], non_blocking=True)
+                        layers[ell * M + m].decode_step(qd[ell][rows], kd[ell][rows], vd[ell][rows],
+                                                        out[ell][rows], None, main=mains[m],
+                                                        side=None if args.single_stream else sides[m])
+                        oh[k, ell][rows].copy_(out[ell][rows], non_blocking=True)
+        join()
+        f1.record(main)
         barrier()
         ms_e2e = max_over_ranks(f0.elapsed_time(f1), ws, dev)
         h2d = L * (qd[0].numel() + kd[0].numel() + vd[0].numel()) * es
@@ -372,6 +406,7 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
                    "rank": w.rank, "chunk": w.chunk, "n_select": w.n_select, "n_outlier": w.n_outlier,
                    "local_window": w.local_window, "v_place": w.v_place, "drift": w.drift,
                    "parallelism": f"replicas x{ws} (batch sharded, no collective)",
+                   "microbatches": M,
                    "layers_share_input_storage": share,
                    "host_values": "one page-locked arena (shadowkv_host_alloc)" if w.v_place == "host" else None,
                    "l2": "inputs larger than L2 (landmarks of one layer exceed 129 MB)"},
@@ -388,7 +423,7 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
         "eq_bandwidth_check": eqbw,
         "clocks": clk,
         "e2e": e2e,
-        "gpu_launches": 5 * L * K,
+        "gpu_launches": 5 * L * M * K,
         "setup_s": setup_s,
     }
     if dev_err:
