@@ -117,27 +117,17 @@ __device__ void topk_threshold(const float* vals, int n, int k, SelShared& sh, i
 #pragma unroll 4
     for (int j = tid; j < n; j += kSelThreads) atomicAdd(&sh.hist[bin_of(vals[j], vmin, invw)], 1);
     __syncthreads();
-    // one warp finds the bin holding the k-th largest: lane l owns bins [64l, 64l+64)
-    if (warp == 0) {
-        constexpr int per = kBins / 32;
-        int cnt = 0;
-#pragma unroll 8
-        for (int b = 0; b < per; ++b) cnt += sh.hist[lane * per + b];
-        int incl = cnt;   // inclusive suffix sum over lanes >= this one
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_down_sync(0xffffffffu, incl, o);
-            if (lane + o < 32) incl += y;
-        }
-        int above = incl - cnt;   // scores in bins of higher lanes
-        if (above < k && k <= incl) {
-            int b = lane * per + per - 1;
-            for (; b > lane * per; --b) {
-                if (above + sh.hist[b] >= k) break;
-                above += sh.hist[b];
-            }
-            sh.bstar = b;
-            sh.above = above;
+    // the bin holding the k-th largest: thread t owns bins 2047-2t and 2046-2t (highest
+    // first); a block-wide prefix sum gives the count in every higher bin
+    static_assert(kBins == 2 * kSelThreads, "two bins per thread");
+    {
+        const int b0 = kBins - 1 - 2 * tid, b1 = b0 - 1;
+        const int h0 = sh.hist[b0], h1 = sh.hist[b1];
+        const int above = block_exscan(h0 + h1, sh, nullptr);
+        if (above < k && k <= above + h0 + h1) {
+            const bool first = above + h0 >= k;
+            sh.bstar = first ? b0 : b1;
+            sh.above = first ? above : above + h0;
         }
     }
     __syncthreads();
@@ -296,15 +286,28 @@ __global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
         const int np = p.nparts;
         const int nrec = p.nru * np;
         const float2* rec = p.part + static_cast<int64_t>(u) * nrec * G;
-        float M = -CUDART_INF_F;
-        for (int r = lane; r < nrec; r += 32) M = fmaxf(M, rec[r * G + warp].x);
-        M = warp_max(M);
-        float S = 0.f;
-        for (int r = lane; r < nrec; r += 32) {
-            const float2 ms = rec[r * G + warp];
-            if (ms.x != -CUDART_INF_F) S += ms.y * __expf(ms.x - M);
+        // running (max, sum) per lane over its records, four loads in flight at a time
+        float m = -CUDART_INF_F, sx = 0.f;
+        for (int r0 = lane; r0 < nrec; r0 += 4 * 32) {
+            float2 x[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = r0 + 32 * i;
+                x[i] = r < nrec ? rec[r * G + warp] : make_float2(-CUDART_INF_F, 0.f);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (x[i].x == -CUDART_INF_F) continue;
+                if (x[i].x > m) {
+                    sx = sx * __expf(m - x[i].x) + x[i].y;
+                    m = x[i].x;
+                } else {
+                    sx += x[i].y * __expf(x[i].x - m);
+                }
+            }
         }
-        S = warp_sum(S);
+        const float M = warp_max(m);
+        const float S = warp_sum(m == -CUDART_INF_F ? 0.f : sx * __expf(m - M));
         if (lane == 0) sh.lse[warp] = M + __logf(S);
     }
     if (u == 0 && tid == 0 && p.sched) *p.sched = 0;   // the scoring kernel of this step is done
@@ -355,14 +358,17 @@ __global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
     const int jlast = sh.jlast;
     const int32_t* ids = p.ids + static_cast<int64_t>(u) * n;
     const int got = compact_selected(vals, n, T, jlast, sh, [&](int pos, int j) {
-        if (pos < K) sSel[pos] = ids[j];
+        if (pos < K) sSel[pos] = j;
     });
     if (got != K) {
         // only non-finite scores can break the count; keep downstream indices valid
         if (tid == 0) set_err(p.err, DEV_ERR_NUMERIC, 312);
-        for (int i = tid; i < K; i += kSelThreads) sSel[i] = ids[i];
+        for (int i = tid; i < K; i += kSelThreads) sSel[i] = i;
         __syncthreads();
     }
+    // positions -> original chunk ids, every load in flight at once
+    for (int i = tid; i < K; i += kSelThreads) sSel[i] = ids[sSel[i]];
+    __syncthreads();
     // 4. index scan against the previous step's selection
     const int t = p.t;
     const int32_t* pids = sPid;
