@@ -54,6 +54,10 @@ struct skv_layer {
     int32_t* ids = nullptr;
     int32_t* out_ids = nullptr;
     float* min_cos = nullptr;
+    // keys and values of the attended set, one block of R rows per unit:
+    // [O*C outlier rows | K*C cache rows (by slot) | loc_cap local rows]
+    void *Kall = nullptr, *Vall = nullptr;
+    int64_t R = 0;
     void *Kout = nullptr, *Vout = nullptr, *Kloc = nullptr, *Vloc = nullptr, *Kc = nullptr, *Vc = nullptr;
     int32_t* sel_ids[2] = {nullptr, nullptr};
     int32_t* sel_slot[2] = {nullptr, nullptr};
@@ -68,6 +72,7 @@ struct skv_layer {
     int32_t* hits_step = nullptr;
     int* err = nullptr;
     CUtensorMap tmA{}, tmB{}, tmL{};
+    CUtensorMap tmKall{};                 // the key blocks, [U*R][128], 128-row boxes (attention)
     int score_ncta = 0, score_nru = 0, score_nparts = 0, sel_smem_cap = 0;
     int32_t* sched = nullptr;
     int64_t t = 0, t_reset = 0;
@@ -338,12 +343,8 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
     if ((rc = alloc(h, &h->L, U * nc * row)) || (rc = alloc_t(h, &h->ids, U * nc)) ||
         (rc = alloc_t(h, &h->out_ids, static_cast<size_t>(U) * std::max(O, 1))) ||
         (rc = alloc_t(h, &h->min_cos, static_cast<size_t>(U) * h->ncand)) ||
-        (rc = alloc(h, &h->Kout, static_cast<size_t>(U) * std::max(O, 1) * kC * row)) ||
-        (rc = alloc(h, &h->Vout, static_cast<size_t>(U) * std::max(O, 1) * kC * row)) ||
-        (rc = alloc(h, &h->Kloc, static_cast<size_t>(U) * h->loc_cap * row)) ||
-        (rc = alloc(h, &h->Vloc, static_cast<size_t>(U) * h->loc_cap * row)) ||
-        (rc = alloc(h, &h->Kc, static_cast<size_t>(U) * K * kC * row)) ||
-        (rc = alloc(h, &h->Vc, static_cast<size_t>(U) * K * kC * row)) ||
+        (rc = alloc(h, &h->Kall, static_cast<size_t>(U) * (static_cast<size_t>(O + K) * kC + h->loc_cap) * row)) ||
+        (rc = alloc(h, &h->Vall, static_cast<size_t>(U) * (static_cast<size_t>(O + K) * kC + h->loc_cap) * row)) ||
         (rc = alloc_t(h, &h->sel_ids[0], static_cast<size_t>(U) * K)) ||
         (rc = alloc_t(h, &h->sel_ids[1], static_cast<size_t>(U) * K)) ||
         (rc = alloc_t(h, &h->sel_slot[0], static_cast<size_t>(U) * K)) ||
@@ -360,6 +361,14 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
         (rc = alloc_t(h, &h->rope_hi, static_cast<size_t>(h->nhi) * kD / 2)) ||
         (rc = alloc_t(h, &h->hits_step, static_cast<size_t>(h->Tmax))) || (rc = alloc_t(h, &h->err, 4)))
         return fail(rc);
+    h->R = static_cast<int64_t>(O + K) * kC + h->loc_cap;
+    {
+        uint8_t* kb = static_cast<uint8_t*>(h->Kall);
+        uint8_t* vb = static_cast<uint8_t*>(h->Vall);
+        const size_t o_off = 0, c_off = static_cast<size_t>(O) * kC * row, l_off = static_cast<size_t>(O + K) * kC * row;
+        h->Kout = kb + o_off; h->Kc = kb + c_off; h->Kloc = kb + l_off;
+        h->Vout = vb + o_off; h->Vc = vb + c_off; h->Vloc = vb + l_off;
+    }
     {
         const int ntot_max = O * kC + K * kC + h->loc_cap;
         const int seg = attn_segment(h->dtype);
@@ -401,7 +410,8 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
         if (launch_transpose_B(B, h->Bt, U, h->r, s)) return fail(SKV_ERR_CUDA);
         if ((rc = make_map(&h->tmA, A, h->r, static_cast<uint64_t>(c.batch) * c.seq_len, 8)) ||
             (rc = make_map(&h->tmB, h->Bt, h->r, static_cast<uint64_t>(U) * kD, 128)) ||
-            (rc = make_map(&h->tmL, h->L, kD, static_cast<uint64_t>(U) * h->n_c, kScTile)))
+            (rc = make_map(&h->tmL, h->L, kD, static_cast<uint64_t>(U) * h->n_c, kScTile)) ||
+            (rc = make_map(&h->tmKall, h->Kall, kD, static_cast<uint64_t>(U) * h->R, 128)))
             return fail(rc);
     }
 
@@ -443,13 +453,13 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
         p.mode = 0;
         if (O > 0) {
             p.list = h->out_ids; p.list_us = O; p.list_cap = O; p.count_const = O;
-            p.dst = h->Kout; p.dst_cap = O; p.dst_us = static_cast<int64_t>(O) * kC * kD;
+            p.dst = h->Kout; p.dst_cap = O; p.dst_us = h->R * kD;
             if (rebuild(p, O)) return fail(SKV_ERR_CUDA);
         }
         const int nloc = h->W / kC;
         if (nloc > 0) {
             p.list = nullptr; p.list_base = h->ncand; p.list_cap = nloc; p.count_const = nloc;
-            p.dst = h->Kloc; p.dst_cap = h->loc_cap / kC; p.dst_us = static_cast<int64_t>(h->loc_cap) * kD;
+            p.dst = h->Kloc; p.dst_cap = h->loc_cap / kC; p.dst_us = h->R * kD;
             if (rebuild(p, nloc)) return fail(SKV_ERR_CUDA);
         }
         GatherParams g{};
@@ -457,13 +467,13 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
         if (O > 0) {
             GatherParams go = g;
             go.list = h->out_ids; go.list_us = O; go.list_cap = O; go.count_const = O; go.dst_cap = O;
-            go.dst = h->Vout; go.dst_us = static_cast<int64_t>(O) * kC * kD;
+            go.dst = h->Vout; go.dst_us = h->R * kD;
             if (launch_gather(go, (O + 7) / 8, s)) return fail(SKV_ERR_CUDA);
         }
         if (nloc > 0) {
             GatherParams gl = g;
             gl.list = nullptr; gl.list_base = h->ncand; gl.list_cap = nloc; gl.count_const = nloc;
-            gl.dst = h->Vloc; gl.dst_cap = h->loc_cap / kC; gl.dst_us = static_cast<int64_t>(h->loc_cap) * kD;
+            gl.dst = h->Vloc; gl.dst_cap = h->loc_cap / kC; gl.dst_us = h->R * kD;
             if (launch_gather(gl, (nloc + 7) / 8, s)) return fail(SKV_ERR_CUDA);
         }
     }
@@ -514,7 +524,7 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     sel.cur_ids = h->sel_ids[(t + 1) & 1]; sel.cur_slot = h->sel_slot[(t + 1) & 1];
     sel.miss_chunk = h->miss_chunk; sel.miss_slot = h->miss_slot; sel.miss_count = h->miss_count;
     sel.hits_step = h->hits_step; sel.k_new = k_new; sel.v_new = v_new; sel.k_loc = h->Kloc; sel.v_loc = h->Vloc;
-    sel.loc_cap = h->loc_cap; sel.W = h->W; sel.es = h->es; sel.err = h->err;
+    sel.loc_cap = h->loc_cap; sel.loc_pitch = h->R; sel.W = h->W; sel.es = h->es; sel.err = h->err;
     if (launch_select_decode(h->dtype, sel, sm)) return SKV_ERR_CUDA;
     if (h->profiling) cudaEventRecord(ev[2], sm);
     // a6 on the side stream: value rows of the missed chunks into their slots
@@ -526,7 +536,7 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     GatherParams g{};
     g.src = h->Vd; g.src_us = h->S * kD; g.list = h->miss_chunk; g.list_us = K; g.list_cap = K;
     g.cnt = h->miss_count; g.dst_idx = h->miss_slot; g.dst_cap = K; g.dst = h->Vc;
-    g.dst_us = static_cast<int64_t>(K) * kC * kD; g.nchunk = h->nchunk; g.es = h->es; g.U = U; g.err = h->err;
+    g.dst_us = h->R * kD; g.nchunk = h->nchunk; g.es = h->es; g.U = U; g.err = h->err;
     const int frc = launch_gather(g, (K + 7) / 8, ss);
     if (frc) return SKV_ERR_CUDA;
     if (h->profiling) cudaEventRecord(ev[6], ss);
@@ -535,7 +545,7 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     RebuildParams rp{};
     rp.mode = 0; rp.U = U; rp.H = h->H; rp.r = h->r; rp.nkb = h->nkb; rp.S = h->S; rp.nchunk = h->nchunk;
     rp.list = h->miss_chunk; rp.list_us = K; rp.list_cap = K; rp.cnt = h->miss_count; rp.dst_idx = h->miss_slot;
-    rp.dst_cap = K; rp.dst = h->Kc; rp.dst_us = static_cast<int64_t>(K) * kC * kD;
+    rp.dst_cap = K; rp.dst = h->Kc; rp.dst_us = h->R * kD;
     rp.rope_lo = h->rope_lo; rp.rope_hi = h->rope_hi; rp.nhi = h->nhi; rp.A = h->A; rp.B = h->B; rp.err = h->err;
     const int gx = (K + kTileChunks - 1) / kTileChunks;
     const int rc = h->dtype == SKV_BF16 ? launch_rebuild_tc(&h->tmA, &h->tmB, rp, gx, sm) : launch_rebuild_f32(rp, gx, sm);
@@ -547,11 +557,14 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     ap.q = q; ap.k_out = h->Kout; ap.v_out = h->Vout; ap.n_out = h->O * kC;
     ap.k_c = h->Kc; ap.v_c = h->Vc; ap.n_cache = K * kC;
     ap.k_loc = h->Kloc; ap.v_loc = h->Vloc; ap.n_loc = h->W + t + 1; ap.loc_cap = h->loc_cap;
+    ap.unit_rows = h->R;
     ap.out = out; ap.part = h->attn_part; ap.counter = h->attn_cnt;
     const int seg = attn_segment(h->dtype);
     ap.nsplit = (ap.n_out + ap.n_cache + ap.n_loc + seg - 1) / seg;
     ap.scale = sp.scale; ap.G = G; ap.U = U; ap.err = h->err;
-    if (launch_attn(h->dtype, ap, sm)) return SKV_ERR_CUDA;
+    if (h->dtype == SKV_BF16 ? launch_attn_tc(&h->tmKall, ap, h->sm_count, sm)
+                             : launch_attn(h->dtype, ap, sm))
+        return SKV_ERR_CUDA;
     if (h->profiling) {
         cudaEventRecord(ev[4], sm);
         h->prof_pending.push_back(ev);
@@ -672,6 +685,21 @@ int shadowkv_export(skv_layer* h, int field, void* dst, size_t bytes, skv_stream
         case SKV_F_HITS_PER_STEP: src = h->hits_step; break;
     }
     if (need == 0) return SKV_OK;
+    // fields inside the per-unit key/value blocks: [U][rows][d] out of rows of pitch R
+    int64_t rows = 0;
+    switch (field) {
+        case SKV_F_K_OUTLIER: case SKV_F_V_OUTLIER: rows = static_cast<int64_t>(h->O) * kC; break;
+        case SKV_F_K_LOCAL: case SKV_F_V_LOCAL: rows = h->loc_cap; break;
+        case SKV_F_K_CACHE: case SKV_F_V_CACHE: rows = static_cast<int64_t>(h->K) * kC; break;
+    }
+    if (rows > 0) {
+        const size_t rb = static_cast<size_t>(kD) * h->es;
+        if (cudaMemcpy2DAsync(dst, rows * rb, src, h->R * rb, rows * rb, h->U, cudaMemcpyDefault, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return SKV_ERR_CUDA;
+        }
+        return SKV_OK;
+    }
     if (cudaMemcpyAsync(dst, src, static_cast<size_t>(need), cudaMemcpyDefault, stream) != cudaSuccess) {
         cudaGetLastError();
         return SKV_ERR_CUDA;

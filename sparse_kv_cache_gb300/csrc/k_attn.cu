@@ -26,14 +26,19 @@ namespace skv {
 
 constexpr int kPartPitch = kD + 4;   // acc[d], max, sum, pad
 
+// rows per unit of each region: the block pitch, or the region's own size when packed
+__device__ __forceinline__ int64_t pitch_out(const AttnParams& p) { return p.unit_rows > 0 ? p.unit_rows : p.n_out; }
+__device__ __forceinline__ int64_t pitch_c(const AttnParams& p) { return p.unit_rows > 0 ? p.unit_rows : p.n_cache; }
+__device__ __forceinline__ int64_t pitch_loc(const AttnParams& p) { return p.unit_rows > 0 ? p.unit_rows : p.loc_cap; }
+
 template <typename T>
 __device__ __forceinline__ const T* row_ptr(const AttnParams& p, const void* out_b, const void* c_b,
                                             const void* loc_b, int u, int tau) {
-    if (tau < p.n_out) return static_cast<const T*>(out_b) + (static_cast<int64_t>(u) * p.n_out + tau) * kD;
+    if (tau < p.n_out) return static_cast<const T*>(out_b) + (static_cast<int64_t>(u) * pitch_out(p) + tau) * kD;
     tau -= p.n_out;
-    if (tau < p.n_cache) return static_cast<const T*>(c_b) + (static_cast<int64_t>(u) * p.n_cache + tau) * kD;
+    if (tau < p.n_cache) return static_cast<const T*>(c_b) + (static_cast<int64_t>(u) * pitch_c(p) + tau) * kD;
     tau -= p.n_cache;
-    return static_cast<const T*>(loc_b) + (static_cast<int64_t>(u) * p.loc_cap + tau) * kD;
+    return static_cast<const T*>(loc_b) + (static_cast<int64_t>(u) * pitch_loc(p) + tau) * kD;
 }
 
 template <typename T, int G>
@@ -221,14 +226,14 @@ __global__ void __launch_bounds__(128) k_attn_bulk(AttnParams p) {
             if (a >= b) continue;
             const __nv_bfloat16 *kb, *vb;
             if (r == 0) {
-                kb = static_cast<const __nv_bfloat16*>(p.k_out) + (static_cast<int64_t>(u) * p.n_out + a) * kD;
-                vb = static_cast<const __nv_bfloat16*>(p.v_out) + (static_cast<int64_t>(u) * p.n_out + a) * kD;
+                kb = static_cast<const __nv_bfloat16*>(p.k_out) + (static_cast<int64_t>(u) * pitch_out(p) + a) * kD;
+                vb = static_cast<const __nv_bfloat16*>(p.v_out) + (static_cast<int64_t>(u) * pitch_out(p) + a) * kD;
             } else if (r == 1) {
-                kb = static_cast<const __nv_bfloat16*>(p.k_c) + (static_cast<int64_t>(u) * p.n_cache + a - bounds[1]) * kD;
-                vb = static_cast<const __nv_bfloat16*>(p.v_c) + (static_cast<int64_t>(u) * p.n_cache + a - bounds[1]) * kD;
+                kb = static_cast<const __nv_bfloat16*>(p.k_c) + (static_cast<int64_t>(u) * pitch_c(p) + a - bounds[1]) * kD;
+                vb = static_cast<const __nv_bfloat16*>(p.v_c) + (static_cast<int64_t>(u) * pitch_c(p) + a - bounds[1]) * kD;
             } else {
-                kb = static_cast<const __nv_bfloat16*>(p.k_loc) + (static_cast<int64_t>(u) * p.loc_cap + a - bounds[2]) * kD;
-                vb = static_cast<const __nv_bfloat16*>(p.v_loc) + (static_cast<int64_t>(u) * p.loc_cap + a - bounds[2]) * kD;
+                kb = static_cast<const __nv_bfloat16*>(p.k_loc) + (static_cast<int64_t>(u) * pitch_loc(p) + a - bounds[2]) * kD;
+                vb = static_cast<const __nv_bfloat16*>(p.v_loc) + (static_cast<int64_t>(u) * pitch_loc(p) + a - bounds[2]) * kD;
             }
             const uint32_t nb = static_cast<uint32_t>(b - a) * kD * 2;
             bulk_g2s(sK + (a - seg0) * kD * 2, kb, nb, &barK);
@@ -382,6 +387,428 @@ static int launch_bulk(const AttnParams& p, cudaStream_t s) {
     cudaFuncSetAttribute(k_attn_bulk<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     k_attn_bulk<G><<<dim3(p.nsplit, p.U), 128, smem, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+// ------------------------------------------------------------ persistent tensor-core form (bf16)
+// The decode step's attention at full size: one CTA per SM walks a contiguous
+// range of the flattened (unit, 128-token segment) sequence, as a pipeline of
+// four roles over a ring of shared-memory stages:
+//  * a producer warp loads each segment's key rows with two 2-D TMA copies
+//    (128-row boxes, 128-byte swizzle) and its value rows with one 1-D bulk
+//    copy -- a unit's outlier, cache and local rows are adjacent in its block --
+//    and writes the unit's query rows;
+//  * one thread issues q.K^T on the tensor cores (M = 128 rows, N = 16 >= G
+//    query heads, K = 128) into a double-buffered accumulator in tensor memory;
+//  * four score-reader warps turn the scores into probabilities against a
+//    running max per head (one row per thread), keeping per-warp running sums;
+//  * four value warps accumulate p.V on the CUDA cores one segment behind,
+//    rescaling when the max moves.
+// Where the range leaves a unit (or ends), a unit the CTA covers whole is
+// normalised and written out; a unit shared with neighbouring CTAs is written
+// as a partial at the slot of the CTA's first segment of it, and the last CTA
+// to take the unit's ticket after the loop merges the partials.
+constexpr int kAWarps = 8;                          // score readers (warps 2..5) + value warps (6..9)
+constexpr int kAKBytes = kBSeg * kD * 2;            // key tile: [2 halves][128 rows][128 B], swizzled
+constexpr int kAQBytes = 4096;                      // query tile: [2 halves][16 rows][128 B], swizzled
+constexpr int kAVBytes = kBSeg * kD * 2;            // value rows, plain
+constexpr int kAStage = kAKBytes + kAQBytes + kAVBytes;
+static_assert(kAStage % 1024 == 0, "stages keep the 1024-byte alignment of the swizzled tiles");
+template <int G> struct AStages { static constexpr int value = G >= 8 ? 2 : 3; };
+
+
+// 32-bit: the launcher checks that ncta * F fits
+__device__ __forceinline__ int aseg_start(int c, int F, int ncta) { return c * F / ncta; }
+// the CTA whose range holds flat segment f: the largest c with aseg_start(c) <= f
+__device__ __forceinline__ int acta_of(int f, int F, int ncta) {
+    int lo = 0, hi = ncta - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (aseg_start(mid, F, ncta) <= f) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+__device__ __forceinline__ void reader_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void value_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+
+template <int G>
+__global__ void __launch_bounds__((kAWarps + 2) * 32, 1) k_attn_tc(const __grid_constant__ CUtensorMap tmK, AttnParams p) {
+    constexpr int S = AStages<G>::value;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smb = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* sRed = reinterpret_cast<float*>(smb + S * kAStage);   // [4 value warps][G][kD]
+    __shared__ uint64_t full[S], empty[S], accf[2], acce[2], pready[2], pfree[2], drain;
+    __shared__ float sP[2][kBSeg * G];                 // probabilities of a segment
+    __shared__ float red_m[2][4][G];                   // per-warp maxima of a segment
+    __shared__ float sCorr[2][G], sMseg[2][G], sLw[2][4][G];   // rescale factor, running max, sums
+    __shared__ uint32_t tmem_slot;
+    __shared__ int s_lastv[2];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int ntot = p.n_out + p.n_cache + p.n_loc;
+    const int nsegu = p.nsplit;                       // segments per unit (= partial pitch)
+    const int F = p.U * nsegu;
+    const int ncta = gridDim.x;
+    const int f0 = aseg_start(blockIdx.x, F, ncta), f1 = aseg_start(blockIdx.x + 1, F, ncta);
+    if (tid == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 2);   // the copies (with their byte count), then the query rows
+            mbar_init(&empty[i], 4);  // the value warps
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accf[b], 1);
+            mbar_init(&acce[b], 4);
+            mbar_init(&pready[b], 4);
+            mbar_init(&pfree[b], 4);
+        }
+        mbar_init(&drain, 1);
+        fence_mbar_init();
+        prefetch_tensormap(&tmK);
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_slot, 32);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer warp
+        constexpr int QW = (G * 16 + 31) / 32;   // 16-byte words of the query rows per lane
+        int it = 0, u = f0 / nsegu, si = f0 - u * nsegu;
+        for (int f = f0; f < f1; ++f, ++it) {
+            const int st = it % S;
+            const int okw = mbar_wait(&empty[st], ((it / S) & 1) ^ 1) ? 1 : 0;
+            if (!__all_sync(0xffffffffu, okw)) {
+                if (lane == 0) set_err(p.err, DEV_ERR_TIMEOUT, 621);
+                break;
+            }
+            const int seg0 = si * kBSeg;
+            const int ua = u;
+            if (++si == nsegu) { si = 0; ++u; }
+            const int nseg = min(kBSeg, ntot - seg0);
+            uint8_t* sK = smb + st * kAStage;
+            uint8_t* sQ = sK + kAKBytes;
+            uint8_t* sV = sQ + kAQBytes;
+            if (lane == 0) {
+                // the unit's block holds the segment's rows contiguously: two 128-row key boxes
+                // (rows past the unit's tokens are read but scored -inf; past the last block the
+                // copy fills zeros) and one bulk copy of the value rows
+                const int row = static_cast<int>(static_cast<int64_t>(ua) * p.unit_rows + seg0);
+                mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(kAKBytes + nseg * kD * 2));
+                tma_load_2d(sK, &tmK, 0, row, &full[st]);
+                tma_load_2d(sK + 16384, &tmK, 64, row, &full[st]);
+                bulk_g2s(sV, static_cast<const __nv_bfloat16*>(p.v_out) + (static_cast<int64_t>(ua) * p.unit_rows + seg0) * kD,
+                         static_cast<uint32_t>(nseg) * kD * 2, &full[st]);
+            }
+            // the unit's query rows g < G (the MMA's other columns are never read), written while
+            // the copies are in flight; the second arrival publishes them
+#pragma unroll
+            for (int k = 0; k < QW; ++k) {
+                const int w = lane + 32 * k, n = w >> 4, c16 = w & 15, kb = c16 >> 3, c = c16 & 7;
+                if (n < G) {
+                    const uint4 qw = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
+                                                                     (static_cast<int64_t>(ua) * G + n) * kD + c16 * 8);
+                    *reinterpret_cast<uint4*>(sQ + kb * 2048 + (n >> 3) * 1024 + (n & 7) * 128 + ((c ^ (n & 7)) << 4)) = qw;
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full[st]);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        constexpr uint32_t idesc = idesc_bf16_f32(kBSeg, 16);
+        int it = 0;
+        for (int f = f0; f < f1; ++f, ++it) {
+            const int st = it % S, b = it & 1;
+            int ok = mbar_wait(&full[st], (it / S) & 1) ? 1 : 0;
+            if (ok) ok = mbar_wait(&acce[b], ((it >> 1) & 1) ^ 1) ? 1 : 0;
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) set_err(p.err, DEV_ERR_TIMEOUT, 623);
+                break;
+            }
+            if (lane == 0) {
+                tc_fence_after();
+                const uint8_t* sK = smb + st * kAStage;
+                const uint8_t* sQ = sK + kAKBytes;
+                uint32_t acc = 0;
+                for (int kb = 0; kb < 2; ++kb)
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t ad = smem_desc_sw128(smem_u32(sK + kb * 16384 + k * 32));
+                        const uint64_t bd = smem_desc_sw128(smem_u32(sQ + kb * 2048 + k * 32));
+                        tc_mma_bf16(tmem + b * 16, ad, bd, idesc, acc);
+                        acc = 1;
+                    }
+                tc_commit(&accf[b]);
+            }
+            __syncwarp();
+        }
+        if (lane == 0) tc_commit(&drain);
+        __syncwarp();
+        (void)mbar_wait(&drain, 0);
+    } else if (warp < 2 + 4) {
+        // ---------------------------------------------------------------- score readers
+        // Four warps, one row (token) per thread: the segment's scores from the accumulator,
+        // the running max per head across the unit's segments, the probabilities into
+        // sP[buf], and per warp a running sum of them.  Segment i + 1 is worked here while the
+        // value warps accumulate segment i.
+        const int rw = warp - 2, quarter = warp & 3;     // TMEM lanes [32q, 32q + 32)
+        const int tl = quarter * 32 + lane;
+        bool ab = false;
+        int cur_u = -1;
+        float m_run[G], lw[G];
+        int it = 0, u = f0 / nsegu, si = f0 - u * nsegu;
+        for (int f = f0; f < f1; ++f, ++it) {
+            const int buf = it & 1;
+            const int seg0 = si * kBSeg;
+            const int nseg = min(kBSeg, ntot - seg0);
+            if (u != cur_u) {
+                cur_u = u;
+#pragma unroll
+                for (int g = 0; g < G; ++g) { m_run[g] = -CUDART_INF_F; lw[g] = 0.f; }
+            }
+            if (!ab && !mbar_wait(&accf[buf], (it >> 1) & 1)) ab = true;
+            tc_fence_after();
+            float v[8];
+            tmem_ld8(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + buf * 16, v);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acce[buf]);
+            float sc[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                sc[g] = tl < nseg ? v[g] * p.scale : -CUDART_INF_F;
+                const float x = warp_max(sc[g]);
+                if (lane == 0) red_m[buf][rw][g] = x;
+            }
+            reader_sync();
+            float corr[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float ms = fmaxf(fmaxf(red_m[buf][0][g], red_m[buf][1][g]), fmaxf(red_m[buf][2][g], red_m[buf][3][g]));
+                const float mnew = fmaxf(m_run[g], ms);
+                corr[g] = (m_run[g] == -CUDART_INF_F) ? 0.f : __expf(m_run[g] - mnew);
+                m_run[g] = mnew;
+            }
+            // the value warps are done with this buffer (segment i - 2)
+            if (!ab && !mbar_wait(&pfree[buf], ((it >> 1) & 1) ^ 1)) ab = true;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float pv = (sc[g] == -CUDART_INF_F) ? 0.f : __expf(sc[g] - m_run[g]);
+                sP[buf][tl * G + g] = pv;
+                lw[g] = lw[g] * corr[g] + warp_sum(pv);
+            }
+            if (lane == 0) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    sLw[buf][rw][g] = lw[g];
+                    if (rw == 0) {
+                        sCorr[buf][g] = corr[g];
+                        sMseg[buf][g] = m_run[g];
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pready[buf]);
+            if (++si == nsegu) { si = 0; ++u; }
+        }
+        if (ab && lane == 0) set_err(p.err, DEV_ERR_TIMEOUT, 624);
+    } else {
+        // ---------------------------------------------------------------- value warps
+        // Four warps, eight half-warps, a lane 8 dims of every head: p . V over the segment's
+        // rows, rescaled when the running max moves.  Where the range leaves a unit (or ends),
+        // a unit this CTA covers whole is normalised and written out; otherwise the state is
+        // written as the partial at the slot of the CTA's first segment of the unit and merged
+        // after the loop.
+        const int pt = tid - 192, pw = warp - 6;
+        const int hl = lane & 15, half = lane >> 4, hw = pw * 2 + half;
+        bool ab = false;
+        int cur_u = -1, ubeg = 0;
+        float acc[G][8];
+        int pend[2] = {-1, -1}, npend = 0;
+
+        auto finish = [&](int u, int slot, int buf) {
+#pragma unroll
+            for (int g = 0; g < G; ++g)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) acc[g][k] += __shfl_down_sync(0xffffffffu, acc[g][k], 16);
+            if (half == 0) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float* r = sRed + (pw * G + g) * kD + hl * 8;
+                    reinterpret_cast<float4*>(r)[0] = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
+                    reinterpret_cast<float4*>(r)[1] = make_float4(acc[g][4], acc[g][5], acc[g][6], acc[g][7]);
+                }
+            }
+            value_sync();
+            const bool whole = slot == 0 && f1 >= (u + 1) * nsegu;
+            float* mypart = p.part + (static_cast<int64_t>(u) * nsegu + slot) * G * kPartPitch;
+            for (int o = pt; o < G * kD; o += 128) {
+                const int g = o / kD, dim = o % kD;
+                const float l = sLw[buf][0][g] + sLw[buf][1][g] + sLw[buf][2][g] + sLw[buf][3][g];
+                const float x = sRed[(0 * G + g) * kD + dim] + sRed[(1 * G + g) * kD + dim] +
+                                sRed[(2 * G + g) * kD + dim] + sRed[(3 * G + g) * kD + dim];
+                if (whole) {
+                    static_cast<__nv_bfloat16*>(p.out)[(static_cast<int64_t>(u) * G + g) * kD + dim] = __float2bfloat16_rn(x / l);
+                } else {
+                    mypart[g * kPartPitch + dim] = x;
+                    if (dim == 0) {
+                        mypart[g * kPartPitch + kD] = sMseg[buf][g];
+                        mypart[g * kPartPitch + kD + 1] = l;
+                    }
+                }
+            }
+            if (!whole && npend < 2) pend[npend++] = u;   // at most the range's first and last unit
+            value_sync();   // sRed is free again
+        };
+
+        int it = 0, u = f0 / nsegu, si = f0 - u * nsegu;
+        for (int f = f0; f < f1; ++f, ++it) {
+            const int st = it % S, buf = it & 1;
+            const int seg0 = si * kBSeg;
+            const int nseg = min(kBSeg, ntot - seg0);
+            if (u != cur_u) {
+                cur_u = u;
+                ubeg = f;
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) acc[g][k] = 0.f;
+            }
+            if (!ab && !mbar_wait(&full[st], (it / S) & 1)) ab = true;      // the value rows
+            if (!ab && !mbar_wait(&pready[buf], (it >> 1) & 1)) ab = true;  // the probabilities
+            const uint8_t* sV = smb + st * kAStage + kAKBytes + kAQBytes;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float c = sCorr[buf][g];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) acc[g][k] *= c;
+            }
+#pragma unroll 4
+            for (int r = hw; r < nseg; r += 8) {
+                float v[8];
+                load8(reinterpret_cast<const __nv_bfloat16*>(sV + r * kD * 2) + hl * 8, v);
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float pg = sP[buf][r * G + g];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) acc[g][k] = fmaf(pg, v[k], acc[g][k]);
+                }
+            }
+            if (si == nsegu - 1 || f == f1 - 1) finish(u, ubeg - u * nsegu, buf);
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&pfree[buf]);
+                mbar_arrive(&empty[st]);
+            }
+            if (++si == nsegu) { si = 0; ++u; }
+        }
+        if (ab) {
+            if (lane == 0) set_err(p.err, DEV_ERR_TIMEOUT, 622);
+        } else if (npend > 0) {
+            // Shared units: once every contributor's partial is in memory the last one to take a
+            // ticket merges.  The contributors are the CTAs whose ranges hold the unit's first
+            // and last segments and every CTA between them (no range is empty: the grid never
+            // exceeds the segment count).
+            __threadfence();   // this CTA's partials before its tickets
+            value_sync();
+            if (pt < npend) {
+                const int uu = pend[pt];
+                const int ncon = acta_of((uu + 1) * nsegu - 1, F, ncta) - acta_of(uu * nsegu, F, ncta) + 1;
+                s_lastv[pt] = (atomicAdd(p.counter + uu, 1) == ncon - 1);
+            }
+            value_sync();
+            for (int i = 0; i < npend; ++i) {
+                if (!s_lastv[i]) continue;   // uniform
+                __threadfence();
+                const int uu = pend[i];
+                const int cA = acta_of(uu * nsegu, F, ncta);
+                const int ncon = acta_of((uu + 1) * nsegu - 1, F, ncta) - cA + 1;
+                const float* parts = p.part + static_cast<int64_t>(uu) * nsegu * G * kPartPitch;
+                // thread pt owns dimension pt of every head: the loads of two contributors for all
+                // heads are in flight at once
+                float M[G], L[G], A[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) { M[g] = -CUDART_INF_F; L[g] = 0.f; A[g] = 0.f; }
+                for (int c0 = 0; c0 < ncon; c0 += 2) {
+                    float mm[2][G], ll[2][G], aa[2][G];
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const int st = aseg_start(cA + c0 + c, F, ncta) - uu * nsegu;
+                        const float* pc = parts + static_cast<int64_t>(st > 0 ? st : 0) * G * kPartPitch;
+#pragma unroll
+                        for (int g = 0; g < G; ++g) {
+                            const bool on = c0 + c < ncon;
+                            mm[c][g] = on ? __ldcg(pc + g * kPartPitch + kD) : -CUDART_INF_F;
+                            ll[c][g] = on ? __ldcg(pc + g * kPartPitch + kD + 1) : 0.f;
+                            aa[c][g] = on ? __ldcg(pc + g * kPartPitch + pt) : 0.f;
+                        }
+                    }
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+#pragma unroll
+                        for (int g = 0; g < G; ++g) {
+                            if (mm[c][g] == -CUDART_INF_F) continue;
+                            if (mm[c][g] > M[g]) {
+                                const float w = (M[g] == -CUDART_INF_F) ? 0.f : __expf(M[g] - mm[c][g]);
+                                A[g] = A[g] * w + aa[c][g];
+                                L[g] = L[g] * w + ll[c][g];
+                                M[g] = mm[c][g];
+                            } else {
+                                const float w = __expf(mm[c][g] - M[g]);
+                                A[g] = fmaf(aa[c][g], w, A[g]);
+                                L[g] = fmaf(ll[c][g], w, L[g]);
+                            }
+                        }
+                }
+#pragma unroll
+                for (int g = 0; g < G; ++g)
+                    static_cast<__nv_bfloat16*>(p.out)[(static_cast<int64_t>(uu) * G + g) * kD + pt] = __float2bfloat16_rn(A[g] / L[g]);
+                if (pt == 0) p.counter[uu] = 0;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 32);
+    }
+}
+
+template <int G>
+static int launch_tc(const CUtensorMap* tmK, const AttnParams& p, int nsm, cudaStream_t s) {
+    const int ntot = p.n_out + p.n_cache + p.n_loc;
+    if (!tmK || p.nsplit != (ntot + kBSeg - 1) / kBSeg || nsm <= 0) return -1;
+    // the block layout, regions adjacent in each block
+    const size_t rb = static_cast<size_t>(kD) * 2;
+    if (p.unit_rows < static_cast<int64_t>(p.n_out) + p.n_cache + p.n_loc ||
+        static_cast<const uint8_t*>(p.k_c) != static_cast<const uint8_t*>(p.k_out) + p.n_out * rb ||
+        static_cast<const uint8_t*>(p.k_loc) != static_cast<const uint8_t*>(p.k_c) + static_cast<size_t>(p.n_cache) * rb ||
+        static_cast<const uint8_t*>(p.v_c) != static_cast<const uint8_t*>(p.v_out) + p.n_out * rb ||
+        static_cast<const uint8_t*>(p.v_loc) != static_cast<const uint8_t*>(p.v_c) + static_cast<size_t>(p.n_cache) * rb)
+        return -1;
+    const int64_t F = static_cast<int64_t>(p.U) * p.nsplit;
+    const int ncta = static_cast<int>(F < nsm ? F : nsm);
+    if (ncta <= 0) return 0;
+    if (F * (ncta + 1) > INT32_MAX || static_cast<int64_t>(p.U) * p.unit_rows > INT32_MAX) return -1;   // 32-bit indexing
+    const size_t smem = static_cast<size_t>(AStages<G>::value) * kAStage + static_cast<size_t>(4) * G * kD * 4 + 1024;
+    cudaFuncSetAttribute(k_attn_tc<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    k_attn_tc<G><<<ncta, (kAWarps + 2) * 32, smem, s>>>(*tmK, p);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_attn_tc(const CUtensorMap* k_all, const AttnParams& p, int nsm, cudaStream_t s) {
+    switch (p.G) {
+        case 1: return launch_tc<1>(k_all, p, nsm, s);
+        case 2: return launch_tc<2>(k_all, p, nsm, s);
+        case 4: return launch_tc<4>(k_all, p, nsm, s);
+        case 8: return launch_tc<8>(k_all, p, nsm, s);
+    }
+    return -1;
 }
 
 int attn_segment(int dtype) { return dtype == 1 ? kBSeg : kAttnSeg; }

@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
         const int row = p.W + p.t;
         const int n16 = kD * p.es / 16;
         if (row < p.loc_cap) {
-            const int64_t off = (static_cast<int64_t>(u) * p.loc_cap + row) * kD * p.es;
+            const int64_t off = (static_cast<int64_t>(u) * p.loc_pitch + row) * kD * p.es;
             const int64_t src = static_cast<int64_t>(u) * kD * p.es;
             if (wt < n16)
                 copy_row16(static_cast<uint8_t*>(p.k_loc) + off, static_cast<const uint8_t*>(p.k_new) + src, n16, wt, 1 << 30);

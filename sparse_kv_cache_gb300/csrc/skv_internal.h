@@ -72,7 +72,7 @@ struct SelectParams {
     int32_t* hits_step;   // [max_new_tokens]
     // append of the new token
     const void* k_new; const void* v_new; void* k_loc; void* v_loc;
-    int loc_cap; int W; int es;
+    int loc_cap; int64_t loc_pitch; int W; int es;   // local rows of unit u start at u * loc_pitch
     int* err;
 };
 int launch_select_decode(int dtype, const SelectParams& p, cudaStream_t s);
@@ -129,6 +129,9 @@ struct AttnParams {
     const void* k_out; const void* v_out; int n_out;    // [U][n_out][d]
     const void* k_c; const void* v_c; int n_cache;      // [U][n_cache][d]
     const void* k_loc; const void* v_loc; int n_loc; int loc_cap;   // [U][loc_cap][d]
+    // > 0: the three regions are slices of per-unit blocks of unit_rows rows (unit u's rows of
+    // every region start at base + u * unit_rows); 0: each region is packed [U][its rows][d]
+    int64_t unit_rows;
     void* out;                     // [U*G][d]
     float* part;                   // [U][nsplit][G][d + 4]
     int* counter;                  // [U]
@@ -136,6 +139,10 @@ struct AttnParams {
     int* err;
 };
 int launch_attn(int dtype, const AttnParams& p, cudaStream_t s);
+// bf16: persistent tensor-core form, one CTA per SM (nsm), nsplit = ceil(tokens / 128); needs the
+// block layout (unit_rows > 0, regions adjacent in each block) and a tensor map over the key
+// blocks, [U * unit_rows][128] (box 64 x 128, 128-byte swizzle)
+int launch_attn_tc(const CUtensorMap* k_all, const AttnParams& p, int nsm, cudaStream_t s);
 int attn_segment(int dtype);   // tokens per attention CTA
 
 }  // namespace skv
