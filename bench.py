@@ -423,7 +423,7 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
         "eq_bandwidth_check": eqbw,
         "clocks": clk,
         "e2e": e2e,
-        "gpu_launches": 5 * L * M * K,
+        "gpu_launches": (6 if w.dtype == "bf16" else 5) * L * M * K,
         "setup_s": setup_s,
     }
     if dev_err:

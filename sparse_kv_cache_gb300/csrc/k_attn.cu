@@ -405,8 +405,8 @@ static int launch_bulk(const AttnParams& p, cudaStream_t s) {
 //    rescaling when the max moves.
 // Where the range leaves a unit (or ends), a unit the CTA covers whole is
 // normalised and written out; a unit shared with neighbouring CTAs is written
-// as a partial at the slot of the CTA's first segment of it, and the last CTA
-// to take the unit's ticket after the loop merges the partials.
+// as a partial at the slot of the CTA's first segment of it, and k_attn_merge,
+// a programmatic dependent launch, merges those partials once the grid is done.
 constexpr int kAWarps = 8;                          // score readers (warps 2..5) + value warps (6..9)
 constexpr int kAKBytes = kBSeg * kD * 2;            // key tile: [2 halves][128 rows][128 B], swizzled
 constexpr int kAQBytes = 4096;                      // query tile: [2 halves][16 rows][128 B], swizzled
@@ -441,7 +441,6 @@ __global__ void __launch_bounds__((kAWarps + 2) * 32, 1) k_attn_tc(const __grid_
     __shared__ float red_m[2][4][G];                   // per-warp maxima of a segment
     __shared__ float sCorr[2][G], sMseg[2][G], sLw[2][4][G];   // rescale factor, running max, sums
     __shared__ uint32_t tmem_slot;
-    __shared__ int s_lastv[2];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int ntot = p.n_out + p.n_cache + p.n_loc;
@@ -472,6 +471,9 @@ __global__ void __launch_bounds__((kAWarps + 2) * 32, 1) k_attn_tc(const __grid_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
+    // the merge kernel that follows may be scheduled beside this grid now; it waits for the
+    // whole grid before it reads a partial
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0) {
         // ---------------------------------------------------------------- producer warp
@@ -621,14 +623,13 @@ __global__ void __launch_bounds__((kAWarps + 2) * 32, 1) k_attn_tc(const __grid_
         // Four warps, eight half-warps, a lane 8 dims of every head: p . V over the segment's
         // rows, rescaled when the running max moves.  Where the range leaves a unit (or ends),
         // a unit this CTA covers whole is normalised and written out; otherwise the state is
-        // written as the partial at the slot of the CTA's first segment of the unit and merged
-        // after the loop.
+        // written as the partial at the slot of the CTA's first segment of the unit, for
+        // k_attn_merge.
         const int pt = tid - 192, pw = warp - 6;
         const int hl = lane & 15, half = lane >> 4, hw = pw * 2 + half;
         bool ab = false;
         int cur_u = -1, ubeg = 0;
         float acc[G][8];
-        int pend[2] = {-1, -1}, npend = 0;
 
         auto finish = [&](int u, int slot, int buf) {
 #pragma unroll
@@ -661,7 +662,6 @@ __global__ void __launch_bounds__((kAWarps + 2) * 32, 1) k_attn_tc(const __grid_
                     }
                 }
             }
-            if (!whole && npend < 2) pend[npend++] = u;   // at most the range's first and last unit
             value_sync();   // sRed is free again
         };
 
@@ -706,70 +706,7 @@ __global__ void __launch_bounds__((kAWarps + 2) * 32, 1) k_attn_tc(const __grid_
             }
             if (++si == nsegu) { si = 0; ++u; }
         }
-        if (ab) {
-            if (lane == 0) set_err(p.err, DEV_ERR_TIMEOUT, 622);
-        } else if (npend > 0) {
-            // Shared units: once every contributor's partial is in memory the last one to take a
-            // ticket merges.  The contributors are the CTAs whose ranges hold the unit's first
-            // and last segments and every CTA between them (no range is empty: the grid never
-            // exceeds the segment count).
-            __threadfence();   // this CTA's partials before its tickets
-            value_sync();
-            if (pt < npend) {
-                const int uu = pend[pt];
-                const int ncon = acta_of((uu + 1) * nsegu - 1, F, ncta) - acta_of(uu * nsegu, F, ncta) + 1;
-                s_lastv[pt] = (atomicAdd(p.counter + uu, 1) == ncon - 1);
-            }
-            value_sync();
-            for (int i = 0; i < npend; ++i) {
-                if (!s_lastv[i]) continue;   // uniform
-                __threadfence();
-                const int uu = pend[i];
-                const int cA = acta_of(uu * nsegu, F, ncta);
-                const int ncon = acta_of((uu + 1) * nsegu - 1, F, ncta) - cA + 1;
-                const float* parts = p.part + static_cast<int64_t>(uu) * nsegu * G * kPartPitch;
-                // thread pt owns dimension pt of every head: the loads of two contributors for all
-                // heads are in flight at once
-                float M[G], L[G], A[G];
-#pragma unroll
-                for (int g = 0; g < G; ++g) { M[g] = -CUDART_INF_F; L[g] = 0.f; A[g] = 0.f; }
-                for (int c0 = 0; c0 < ncon; c0 += 2) {
-                    float mm[2][G], ll[2][G], aa[2][G];
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        const int st = aseg_start(cA + c0 + c, F, ncta) - uu * nsegu;
-                        const float* pc = parts + static_cast<int64_t>(st > 0 ? st : 0) * G * kPartPitch;
-#pragma unroll
-                        for (int g = 0; g < G; ++g) {
-                            const bool on = c0 + c < ncon;
-                            mm[c][g] = on ? __ldcg(pc + g * kPartPitch + kD) : -CUDART_INF_F;
-                            ll[c][g] = on ? __ldcg(pc + g * kPartPitch + kD + 1) : 0.f;
-                            aa[c][g] = on ? __ldcg(pc + g * kPartPitch + pt) : 0.f;
-                        }
-                    }
-#pragma unroll
-                    for (int c = 0; c < 2; ++c)
-#pragma unroll
-                        for (int g = 0; g < G; ++g) {
-                            if (mm[c][g] == -CUDART_INF_F) continue;
-                            if (mm[c][g] > M[g]) {
-                                const float w = (M[g] == -CUDART_INF_F) ? 0.f : __expf(M[g] - mm[c][g]);
-                                A[g] = A[g] * w + aa[c][g];
-                                L[g] = L[g] * w + ll[c][g];
-                                M[g] = mm[c][g];
-                            } else {
-                                const float w = __expf(mm[c][g] - M[g]);
-                                A[g] = fmaf(aa[c][g], w, A[g]);
-                                L[g] = fmaf(ll[c][g], w, L[g]);
-                            }
-                        }
-                }
-#pragma unroll
-                for (int g = 0; g < G; ++g)
-                    static_cast<__nv_bfloat16*>(p.out)[(static_cast<int64_t>(uu) * G + g) * kD + pt] = __float2bfloat16_rn(A[g] / L[g]);
-                if (pt == 0) p.counter[uu] = 0;
-            }
-        }
+        if (ab && lane == 0) set_err(p.err, DEV_ERR_TIMEOUT, 622);
     }
     tc_fence_before();
     __syncthreads();
@@ -777,6 +714,58 @@ __global__ void __launch_bounds__((kAWarps + 2) * 32, 1) k_attn_tc(const __grid_
         tc_fence_after();
         tmem_dealloc(tmem, 32);
     }
+}
+
+// Merges the partials of every unit shared by several CTAs of k_attn_tc (ncta CTAs):
+// one CTA per unit, a thread per dimension, every contributor's (max, sum, p.V) of all
+// heads loaded at once.  Launched as a programmatic dependent of k_attn_tc: its CTAs may
+// become resident early and wait for the whole attention grid before reading.
+template <int G>
+__global__ void __launch_bounds__(kD) k_attn_merge(AttnParams p, int ncta) {
+    const int u = blockIdx.x, dim = threadIdx.x;
+    const int nsegu = p.nsplit, F = p.U * nsegu;
+    const int cA = acta_of(u * nsegu, F, ncta);
+    const int ncon = acta_of((u + 1) * nsegu - 1, F, ncta) - cA + 1;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (ncon <= 1) return;   // covered whole by one CTA, which wrote the output itself
+    const float* parts = p.part + static_cast<int64_t>(u) * nsegu * G * kPartPitch;
+    float M[G], L[G], A[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) { M[g] = -CUDART_INF_F; L[g] = 0.f; A[g] = 0.f; }
+    for (int c0 = 0; c0 < ncon; c0 += 2) {
+        float mm[2][G], ll[2][G], aa[2][G];   // two contributors' loads of all heads in flight
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int st = aseg_start(cA + c0 + c, F, ncta) - u * nsegu;
+            const float* pc = parts + static_cast<int64_t>(st > 0 ? st : 0) * G * kPartPitch;
+            const bool on = c0 + c < ncon;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                mm[c][g] = on ? __ldcg(pc + g * kPartPitch + kD) : -CUDART_INF_F;
+                ll[c][g] = on ? __ldcg(pc + g * kPartPitch + kD + 1) : 0.f;
+                aa[c][g] = on ? __ldcg(pc + g * kPartPitch + dim) : 0.f;
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                if (mm[c][g] == -CUDART_INF_F) continue;
+                if (mm[c][g] > M[g]) {
+                    const float w = (M[g] == -CUDART_INF_F) ? 0.f : __expf(M[g] - mm[c][g]);
+                    A[g] = A[g] * w + aa[c][g];
+                    L[g] = L[g] * w + ll[c][g];
+                    M[g] = mm[c][g];
+                } else {
+                    const float w = __expf(mm[c][g] - M[g]);
+                    A[g] = fmaf(aa[c][g], w, A[g]);
+                    L[g] = fmaf(ll[c][g], w, L[g]);
+                }
+            }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+        static_cast<__nv_bfloat16*>(p.out)[(static_cast<int64_t>(u) * G + g) * kD + dim] = __float2bfloat16_rn(A[g] / L[g]);
 }
 
 template <int G>
@@ -798,7 +787,22 @@ static int launch_tc(const CUtensorMap* tmK, const AttnParams& p, int nsm, cudaS
     const size_t smem = static_cast<size_t>(AStages<G>::value) * kAStage + static_cast<size_t>(4) * G * kD * 4 + 1024;
     cudaFuncSetAttribute(k_attn_tc<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     k_attn_tc<G><<<ncta, (kAWarps + 2) * 32, smem, s>>>(*tmK, p);
-    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+    if (cudaGetLastError() != cudaSuccess) return -1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.U);
+    cfg.blockDim = dim3(kD);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, k_attn_merge<G>, p, ncta) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    return 0;
 }
 
 int launch_attn_tc(const CUtensorMap* k_all, const AttnParams& p, int nsm, cudaStream_t s) {
