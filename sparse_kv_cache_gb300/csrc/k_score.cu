@@ -205,6 +205,9 @@ __global__ void __launch_bounds__(192, 1) k_score_tc(const __grid_constant__ CUt
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
+    // the set-up above overlapped the previous kernel; everything below reads its results
+    pdl_wait();
+    pdl_trigger();
 
     if (warp == 0) {
         // ------------------------------------------------ producer warp: claims runs, writes each
@@ -389,8 +392,11 @@ template <int G>
 static int launch_tc(const CUtensorMap* tmL, const ScoreParams& p, int ncta, cudaStream_t s) {
     const int smem = kScStages * (32768 + 4096) + 1024;
     cudaFuncSetAttribute(k_score_tc<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    k_score_tc<G><<<ncta, 192, smem, s>>>(*tmL, p);
-    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+    if (launch_pdl(k_score_tc<G>, dim3(ncta), dim3(192), smem, s, *tmL, p) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    return 0;
 }
 
 template <typename T, int G>

@@ -250,6 +250,8 @@ __global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
     __shared__ SelShared sh;
     const int u = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n = p.n, K = p.k;
+    pdl_wait();      // the scores of this step
+    pdl_trigger();
     float* vals = (n <= p.smem_cap) ? reinterpret_cast<float*>(dsm) : p.vbuf + static_cast<int64_t>(u) * n;
     const int cap_f = (n <= p.smem_cap) ? ((n + 3) & ~3) : 0;
     int32_t* sSel = reinterpret_cast<int32_t*>(dsm) + cap_f;
@@ -481,8 +483,11 @@ int launch_select_decode(int dtype, const SelectParams& p, cudaStream_t s) {
         default: return -1;
     }
     cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    fn<<<p.U, kSelThreads, smem, s>>>(p);
-    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+    if (launch_pdl(fn, dim3(p.U), dim3(kSelThreads), smem, s, p) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    return 0;
 }
 
 int launch_select_outliers(const SelectParams& p, cudaStream_t s) {

@@ -136,6 +136,30 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     }
 }
 
+// ----------------------------------------------------------------- programmatic dependent launch
+// Wait for the grids this one depends on (returns at once when the launch did not allow
+// programmatic overlap) / let the grid that follows be scheduled before this one ends.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch that lets the kernel start while the previous kernel in the stream finishes; the
+// kernel must call pdl_wait() before it touches anything an earlier kernel writes or reads.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, static_cast<Args&&>(args)...);
+}
+
 // ----------------------------------------------------------------- bulk copies (TMA)
 // 1-D bulk copy global -> shared, completion counted on `bar` (bytes % 16 == 0,
 // both addresses 16-byte aligned).
