@@ -478,6 +478,7 @@ __global__ void __launch_bounds__((kAWarps + 2) * 32, 1) k_attn_tc(const __grid_
     if (warp == 0) {
         // ---------------------------------------------------------------- producer warp
         constexpr int QW = (G * 16 + 31) / 32;   // 16-byte words of the query rows per lane
+        const uint64_t pol = l2_evict_first();   // read once per step
         int it = 0, u = f0 / nsegu, si = f0 - u * nsegu;
         for (int f = f0; f < f1; ++f, ++it) {
             const int st = it % S;
@@ -499,10 +500,10 @@ __global__ void __launch_bounds__((kAWarps + 2) * 32, 1) k_attn_tc(const __grid_
                 // copy fills zeros) and one bulk copy of the value rows
                 const int row = static_cast<int>(static_cast<int64_t>(ua) * p.unit_rows + seg0);
                 mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(kAKBytes + nseg * kD * 2));
-                tma_load_2d(sK, &tmK, 0, row, &full[st]);
-                tma_load_2d(sK + 16384, &tmK, 64, row, &full[st]);
-                bulk_g2s(sV, static_cast<const __nv_bfloat16*>(p.v_out) + (static_cast<int64_t>(ua) * p.unit_rows + seg0) * kD,
-                         static_cast<uint32_t>(nseg) * kD * 2, &full[st]);
+                tma_load_2d_hint(sK, &tmK, 0, row, &full[st], pol);
+                tma_load_2d_hint(sK + 16384, &tmK, 64, row, &full[st], pol);
+                bulk_g2s_hint(sV, static_cast<const __nv_bfloat16*>(p.v_out) + (static_cast<int64_t>(ua) * p.unit_rows + seg0) * kD,
+                              static_cast<uint32_t>(nseg) * kD * 2, &full[st], pol);
             }
             // the unit's query rows g < G (the MMA's other columns are never read), written while
             // the copies are in flight; the second arrival publishes them

@@ -214,6 +214,7 @@ __global__ void __launch_bounds__(192, 1) k_score_tc(const __grid_constant__ CUt
         // stage's query tile (rows g < G; the MMA's other columns are never read) and issues the
         // landmark copies
         constexpr int QW = (G * 16 + 31) / 32;   // 16-byte words of the query rows per lane
+        const uint64_t pol = l2_evict_first();   // read once per step
         int it = 0;
         int next = (lane == 0) ? atomicAdd(p.sched, 1) : 0;
         next = __shfl_sync(0xffffffffu, next, 0);
@@ -275,8 +276,8 @@ __global__ void __launch_bounds__(192, 1) k_score_tc(const __grid_constant__ CUt
                     t.last = (j + kScTile >= e);
                     stile[s] = t;
                     mbar_arrive_expect_tx(&full[s], 32768);
-                    tma_load_2d(st, &tmL, 0, static_cast<int>(j), &full[s]);
-                    tma_load_2d(st + 16384, &tmL, 64, static_cast<int>(j), &full[s]);
+                    tma_load_2d_hint(st, &tmL, 0, static_cast<int>(j), &full[s], pol);
+                    tma_load_2d_hint(st + 16384, &tmL, 64, static_cast<int>(j), &full[s], pol);
                 }
                 __syncwarp();
             }
