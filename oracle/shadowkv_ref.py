@@ -204,23 +204,43 @@ def attend(q_group: np.ndarray, K: np.ndarray, V: np.ndarray) -> np.ndarray:
 
 def round_to_storage(x: np.ndarray, storage: str | None) -> np.ndarray:
     """Value of x once stored in the configured storage dtype: "bf16" rounds
-    to bfloat16 (nearest even), "f32" to float32, None keeps float64."""
+    to bfloat16 (nearest even), "f32" to float32, "e5m2" to the 8-bit float
+    with 5 exponent and 2 mantissa bits, None keeps float64."""
     if storage is None:
         return np.asarray(x, np.float64)
     if storage == "bf16":
         return bf16_round(x)
     if storage == "f32":
         return np.asarray(x, np.float32).astype(np.float64)
+    if storage == "e5m2":
+        return e5m2_round(x)
     raise ValueError(storage)
 
 
+def key_storage(dtype: str | None) -> str | None:
+    """Storage of the keys the method keeps for a configuration dtype.  In the
+    "fp8" configuration (summary page, section 5, "Precision sensitivity":
+    ShadowKV run with float8 e5m2) landmarks and values are stored in e5m2
+    while the keys, A and B stay bf16 (reading: the pages keep the factors at
+    higher precision; the rebuilt keys are formed like the bf16 ones)."""
+    return "bf16" if dtype == "fp8" else dtype
+
+
+def value_storage(dtype: str | None) -> str | None:
+    """Storage of the values (and of the landmarks) for a configuration dtype."""
+    return "e5m2" if dtype == "fp8" else dtype
+
+
 def attend_on_index_set(q_group, A_b, B_bh, V_bh, outlier_ids, sel_ids, k_local, v_local,
-                        C: int, base: float, storage: str | None = None) -> np.ndarray:
+                        C: int, base: float, storage: str | None = None,
+                        v_storage: str | None = None) -> np.ndarray:
     """Attention over [K_outlier; RoPE(K_sparse); K_local] for given index sets
     (summary page, "Assembly of the final sparse KV cache").  Keys of outlier
     and selected chunks are rebuilt here in float64 from A and B; with
     ``storage`` set, the keys the method keeps (outlier keys, rebuilt keys,
-    local-window keys) take the value they have once stored in that dtype."""
+    local-window keys) take the value they have once stored in that dtype, and
+    with ``v_storage`` set the local-window values likewise (context values
+    arrive already stored)."""
     A_b = np.asarray(A_b, np.float64)
     V_bh = np.asarray(V_bh, np.float64)
     to = chunk_tokens(outlier_ids, C)
@@ -229,7 +249,8 @@ def attend_on_index_set(q_group, A_b, B_bh, V_bh, outlier_ids, sel_ids, k_local,
     K = np.concatenate([round_to_storage(rebuild_keys(A_b[to], B_bh, to, base), storage),
                         round_to_storage(rebuild_keys(A_b[ts], B_bh, ts, base), storage),
                         round_to_storage(np.asarray(k_local, np.float64).reshape(-1, d), storage)])
-    V = np.concatenate([V_bh[to], V_bh[ts], np.asarray(v_local, np.float64).reshape(-1, d)])
+    V = np.concatenate([V_bh[to], V_bh[ts],
+                        round_to_storage(np.asarray(v_local, np.float64).reshape(-1, d), v_storage)])
     return attend(q_group, K, V)
 
 
@@ -308,6 +329,33 @@ def bf16_round(x: np.ndarray) -> np.ndarray:
     lsb = (u >> 16) & 1
     u = (u + 0x7FFF + lsb) >> 16 << 16
     return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+E5M2_MAX = 57344.0          # 1.75 * 2^15, the largest finite e5m2 value
+E5M2_MIN_NORMAL = 2.0 ** -14
+E5M2_MIN_SUB = 2.0 ** -16   # subnormal spacing
+
+
+def e5m2_round(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to the nearest e5m2 value (1 sign, 5 exponent bits
+    with bias 15, 2 mantissa bits; ties to the even mantissa), saturating at
+    the largest finite magnitude; returned as float64.  Between 2^e and
+    2^(e+1) (normal range) the spacing is 2^(e-2); below 2^-14 it is 2^-16."""
+    x = np.asarray(x, np.float64)
+    a = np.abs(x)
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    # guard log2 rounding at exact powers of two
+    e = np.where(2.0 ** e > a, e - 1, e)
+    e = np.where(2.0 ** (e + 1) <= a, e + 1, e)
+    q = np.where(a >= E5M2_MIN_NORMAL, 2.0 ** (e - 2), E5M2_MIN_SUB)
+    m = a / q                                  # exact: q is a power of two
+    r = np.floor(m)
+    frac = m - r
+    up = (frac > 0.5) | ((frac == 0.5) & (np.mod(r, 2) == 1))
+    r = np.where(up, r + 1, r)
+    y = np.minimum(r * q, E5M2_MAX)
+    return np.where(np.isfinite(x), np.copysign(y, x), x)
 
 
 def near_tie_band(scores: np.ndarray, k: int, rel: float = 1e-4):

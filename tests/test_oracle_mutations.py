@@ -33,6 +33,15 @@ def _attend_scale_1_over_d(q_group, K, V):
     return ref.softmax_rows(s) @ np.asarray(V, np.float64)
 
 
+def _e5m2_ties_away(x):
+    x = np.asarray(x, np.float64)
+    a = np.abs(x)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    q = np.where(a >= 2.0 ** -14, 2.0 ** (e - 2), 2.0 ** -16)
+    y = np.minimum(np.floor(a / q + 0.5) * q, 57344.0)
+    return np.copysign(y, x)
+
+
 def _select_raw_logit_max(q_group, landmarks, ids, k):
     P = np.asarray(q_group) @ np.asarray(landmarks).T
     S2 = P.max(axis=0)
@@ -82,6 +91,7 @@ def _hit_miss_swapped(prev, cur):
 _orig_hit_miss = ref.hit_miss
 
 MUTANTS = [
+    ("e5m2_round", _e5m2_ties_away, [pins.test_e5m2_round_hand_values]),
     ("apply_rope", _rope_wrong_sign, [pins.test_rope_closed_form_basis_vectors]),
     ("apply_rope", _rope_interleaved, [pins.test_rope_closed_form_basis_vectors,
                                        pins.test_full_rank_full_budget_equals_dense_causal_attention]),

@@ -289,3 +289,81 @@ def test_storage_rounding_of_kept_keys():
     assert 0 < np.max(np.abs(a - b)) < 1e-5 < np.max(np.abs(a - d)) < 0.1
     x = np.array([1.0 + 2 ** -9, 3.0, -2.0 ** -130])
     np.testing.assert_array_equal(ref.round_to_storage(x, "bf16"), ref.bf16_round(x))
+
+
+# e5m2: 1 sign bit, 5 exponent bits (bias 15), 2 mantissa bits.  Values worked out by hand from
+# that definition: spacing 2^(e-2) in [2^e, 2^(e+1)), 2^-16 below 2^-14, ties to the even
+# mantissa, the largest finite value 1.75 * 2^15 = 57344.
+E5M2_CASES = [
+    (1.0, 1.0), (1.1, 1.0), (1.125, 1.0),        # tie between mantissas 00 and 01 -> 00
+    (1.375, 1.5),                                # tie between 01 and 10 -> 10
+    (1.4, 1.5), (1.74, 1.75), (1.9, 2.0),
+    (3.3, 3.5), (-0.3, -0.3125),                 # [0.25, 0.5) spacing 1/16
+    (57344.0, 57344.0), (60000.0, 57344.0),      # saturation at the largest finite value
+    (2.0 ** -14, 2.0 ** -14),                    # smallest normal
+    (2.0 ** -16, 2.0 ** -16),                    # smallest subnormal
+    (2.0 ** -17, 0.0),                           # tie between 0 and 2^-16 -> 0 (even)
+    (3 * 2.0 ** -17, 2.0 ** -15),                # tie between 1 and 2 subnormal steps -> 2
+    (0.0, 0.0),
+]
+
+
+def test_e5m2_round_hand_values():
+    got = ref.e5m2_round(np.array([x for x, _ in E5M2_CASES]))
+    for (x, want), g in zip(E5M2_CASES, got):
+        assert g == want, (x, want, g)
+
+
+def test_e5m2_grid_is_closed_and_monotone():
+    # every value of the grid between 2^-16 and 57344 rounds to itself, and rounding is monotone
+    grid = [0.0] + [k * 2.0 ** -16 for k in range(1, 4)]
+    for e in range(-14, 16):
+        grid += [(1 + m / 4) * 2.0 ** e for m in range(4)]
+    grid = np.array(sorted(set(grid)))
+    np.testing.assert_array_equal(ref.e5m2_round(grid), grid)
+    np.testing.assert_array_equal(ref.e5m2_round(-grid), -grid)
+    x = np.sort(np.random.default_rng(3).uniform(-60000, 60000, 20000))
+    assert np.all(np.diff(ref.e5m2_round(x)) >= 0)
+    assert len(grid) == 1 + 3 + 30 * 4   # zero, 3 subnormals, 30 binades of 4: all finite e5m2 >= 0
+
+
+def test_e5m2_round_agrees_with_torch_in_range():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal(20000) * 10.0 ** rng.integers(-4, 4, 20000)
+    x = x[np.abs(x) < 57000]
+    want = torch.tensor(x.astype(np.float32)).to(torch.float8_e5m2).double().numpy()
+    np.testing.assert_array_equal(ref.e5m2_round(x.astype(np.float32).astype(np.float64)), want)
+
+
+def test_bf16_is_three_e5m2_terms():
+    # The fp8 scorer feeds the bf16 query to an e5m2 tensor-core product as three e5m2 terms
+    # t1 = e5m2(q), t2 = e5m2(q - t1), t3 = e5m2(q - t1 - t2): each term holds the next three
+    # significant bits, so the sum is q exactly when the last residual is still a multiple of
+    # e5m2's smallest step, i.e. for 2^-9 <= |q| <= 57344.
+    rng = np.random.default_rng(5)
+    q = ref.bf16_round(rng.standard_normal(50000) * 2.0 ** rng.integers(-6, 8, 50000))
+    q = q[(np.abs(q) >= 2.0 ** -9) & (np.abs(q) <= 57344)]
+    t1 = ref.e5m2_round(q)
+    t2 = ref.e5m2_round(q - t1)
+    t3 = ref.e5m2_round(q - t1 - t2)
+    np.testing.assert_array_equal(t1 + t2 + t3, q)
+    # Hence the scorer scales each head's query by 2^s, the largest power of two with
+    # max|q| * 2^s <= 2^14, before splitting: every component down to max|q| * 2^-22 is exact,
+    # and a smaller one is off by less than 2^-16 * 2^-s.
+    for _ in range(200):
+        v = ref.bf16_round(rng.standard_normal(128) * 2.0 ** rng.integers(-20, 10))
+        sc = 2.0 ** np.floor(np.log2(2.0 ** 14 / np.max(np.abs(v))))
+        x = v * sc
+        t1 = ref.e5m2_round(x)
+        t2 = ref.e5m2_round(x - t1)
+        t3 = ref.e5m2_round(x - t1 - t2)
+        err = np.abs((t1 + t2 + t3) - x)
+        big = np.abs(v) >= np.max(np.abs(v)) * 2.0 ** -22
+        assert np.all(err[big] == 0) and np.all(err < 2.0 ** -16)
+
+
+def test_fp8_storage_readings():
+    assert ref.key_storage("fp8") == "bf16" and ref.value_storage("fp8") == "e5m2"
+    assert ref.key_storage("bf16") == "bf16" and ref.value_storage("bf16") == "bf16"
+    x = np.array([1.1, -0.3, 2.0 ** -17])
+    np.testing.assert_array_equal(ref.round_to_storage(x, "e5m2"), [1.0, -0.3125, 0.0])

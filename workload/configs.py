@@ -28,7 +28,8 @@ class Workload:
     n_outlier: int        # O outlier chunks per KV head
     local_window: int     # W tokens kept exact (multiple of C)
     steps: int            # decode steps
-    dtype: str            # "f32" or "bf16" (storage); accumulation is fp32 on the GPU
+    dtype: str            # "f32", "bf16" or "fp8" (storage; fp8: e5m2 landmarks and values, bf16
+                          # keys and factors); accumulation is fp32 on the GPU
     v_place: str          # "hbm" or "host"
     drift: float = 0.9    # AR(1) coefficient of the query between steps
     seed: int = 0

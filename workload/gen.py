@@ -38,7 +38,13 @@ def _gen(w: Workload, layer: int, purpose: str, device) -> torch.Generator:
 
 
 def storage_dtype(w: Workload) -> torch.dtype:
+    """Storage of A, B, the queries and the new keys and values as handed in."""
     return torch.float32 if w.dtype == "f32" else torch.bfloat16
+
+
+def value_dtype(w: Workload) -> torch.dtype:
+    """Storage of the context values: float8 e5m2 in the "fp8" configuration."""
+    return torch.float8_e5m2 if w.dtype == "fp8" else storage_dtype(w)
 
 
 def ar1_scan(e: torch.Tensor, rho: float, dim: int) -> torch.Tensor:
@@ -89,7 +95,7 @@ def make_B(w: Workload, layer: int, device="cpu") -> torch.Tensor:
 
 def make_V(w: Workload, layer: int, device="cpu") -> torch.Tensor:
     g = _gen(w, layer, "V", device)
-    dt = storage_dtype(w)
+    dt = value_dtype(w)
     V = torch.empty((w.batch, w.n_kv_heads, w.seq_len, w.head_dim), dtype=dt, device=device)
     # fill one (b, h) slab at a time to bound the fp32 temporary
     for b in range(w.batch):
