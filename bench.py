@@ -35,6 +35,10 @@ from workload import ALL, LLAMA_128K, Workload  # noqa: E402
 SCORE_TRAFFIC = {"source_sha256": "1f96b4682ac28cf2c31680e6d4c4a093f1f6990af7e78e3803252981285f75fb",
                  "seq_len": 131072, "dtype": "bf16", "bytes_per_unit": (133892096 + 4653568) / 32}
 
+# kernels one layer's decode step launches: score, select, gather, rebuild, attention, merge;
+# the e5m2 configuration adds the query split ahead of the scorer
+LAUNCHES_PER_LAYER = {"bf16": 6, "fp8": 7}
+
 METRIC = "sparse decode-attention tokens/s and HBM GB/s (% of 8 TB/s) at 128K, 1×GB300"
 UNIT = "tokens/s"
 
@@ -49,6 +53,8 @@ def parse():
     ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count")
     ap.add_argument("--batch", type=int, default=0)
     ap.add_argument("--v-place", default="", choices=["", "hbm", "host"])
+    ap.add_argument("--dtype", default="", choices=["", "bf16", "fp8"],
+                    help="storage: bf16, or fp8 (e5m2 landmarks and values, bf16 keys and factors)")
     ap.add_argument("--drift", type=float, default=-1.0)
     ap.add_argument("--share-storage", default="auto", choices=["auto", "yes", "no"],
                     help="reuse one layer's A/B/V for every layer (state stays per layer)")
@@ -70,6 +76,10 @@ def workload_from(args) -> Workload:
         kw["batch"] = args.batch
     if args.v_place:
         kw["v_place"] = args.v_place
+    if args.dtype:
+        kw["dtype"] = args.dtype
+        if args.dtype == "fp8":
+            kw["name"] = w.name + "-fp8"
     if args.drift >= 0:
         kw["drift"] = args.drift
     return w.with_(**kw) if kw else w
@@ -182,7 +192,7 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
     import torch.distributed as dist
 
     import sparse_kv_cache_gb300 as skv
-    from workload import make_A, make_B, make_decode_inputs, make_V, storage_dtype
+    from workload import make_A, make_B, make_decode_inputs, make_V, storage_dtype, value_dtype
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -193,9 +203,10 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
     total_steps = W + passes * K
     w = w.with_(seed=replica_seed(w.seed, rank), steps=total_steps)
     L = w.layers
-    dt = storage_dtype(w)
-    es = 2 if w.dtype == "bf16" else 4
-    v_bytes = w.batch * w.n_kv_heads * w.seq_len * w.head_dim * es
+    dt, vdt = storage_dtype(w), value_dtype(w)   # keys, factors, q, out / values
+    es = 4 if w.dtype == "f32" else 2
+    es_v = 1 if w.dtype == "fp8" else es          # values and landmarks
+    v_bytes = w.batch * w.n_kv_heads * w.seq_len * w.head_dim * es_v
     share = args.share_storage == "yes"
     if args.share_storage == "auto" and w.v_place == "host":
         share = mem_available_gb() < 1.3 * L * v_bytes / 1e9 + 16
@@ -209,7 +220,7 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
     if w.v_place == "host":
         # one page-locked arena for every layer's values (large allocations keep GPU translations few)
         per = w.batch * w.n_kv_heads * w.seq_len * w.head_dim
-        arena = skv.HostBuffer((n_data * per,), dt)
+        arena = skv.HostBuffer((n_data * per,), vdt)
     # one (main, side) stream pair per micro-batch; the value fetch (link-bound) goes first
     mains = [torch.cuda.Stream(dev) for _ in range(M)]
     sides = [torch.cuda.Stream(dev, priority=-10) for _ in range(M)]
@@ -317,7 +328,7 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
     phase_n = {ph: sum(s["phase_launches"][ph] for s in st2) for ph in skv.PHASES}
     score_us = 1000.0 * phase_ms["score"] / max(1, phase_n["score"])
     # one scorer launch covers one micro-batch: landmarks + queries of its units
-    score_bytes = (w.units // M) * (w.n_selectable + w.group) * w.head_dim * es
+    score_bytes = (w.units // M) * (w.n_selectable * es_v + w.group * es) * w.head_dim
     achieved = score_bytes / (score_us * 1e-6) / 1e9
     score_traffic = score_traffic_per_launch(w.with_(batch=bm))
     peak, peak_kind = measured_peaks()
@@ -361,8 +372,8 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
     # host-link bandwidth, measured live: page-locked host -> HBM copy of 256 MB from the value arena
     b_link = None
     if arena is not None:
-        n = min(arena.tensor.numel(), (256 << 20) // es)
-        dbuf = torch.empty(n, dtype=dt, device=dev)
+        n = min(arena.tensor.numel(), (256 << 20) // es_v)
+        dbuf = torch.empty(n, dtype=vdt, device=dev)
         src = arena.tensor.view(-1)[:n]
         dbuf.copy_(src, non_blocking=True)
         torch.cuda.synchronize()
@@ -372,7 +383,7 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
             dbuf.copy_(src, non_blocking=True)
         c1.record()
         torch.cuda.synchronize()
-        b_link = 3 * n * es / (c0.elapsed_time(c1) * 1e-3) / 1e9
+        b_link = 3 * n * es_v / (c0.elapsed_time(c1) * 1e-3) / 1e9
         del dbuf
     # the pages' equivalent-bandwidth model with the measured hit rate and bandwidths: predicted step time
     peak_gbs, _ = measured_peaks()
@@ -400,7 +411,8 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
     line = {
         "metric": METRIC, "value": tokens_s, "unit": UNIT, "n_gpus": ws, "steps": K, "warmup": W,
         "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": w.dtype, "data": "synthetic (seeded generator; Llama-3.1-8B attention shape)",
+        "dtype": "bf16+e5m2" if w.dtype == "fp8" else w.dtype,
+        "data": "synthetic (seeded generator; Llama-3.1-8B attention shape)",
         "config": {"workload": w.name, "layers": L, "batch_per_gpu": w.batch, "seq_len": w.seq_len,
                    "n_kv_heads": w.n_kv_heads, "n_q_heads": w.n_q_heads, "head_dim": w.head_dim,
                    "rank": w.rank, "chunk": w.chunk, "n_select": w.n_select, "n_outlier": w.n_outlier,
@@ -423,7 +435,7 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
         "eq_bandwidth_check": eqbw,
         "clocks": clk,
         "e2e": e2e,
-        "gpu_launches": (6 if w.dtype == "bf16" else 5) * L * M * K,
+        "gpu_launches": LAUNCHES_PER_LAYER[w.dtype] * L * M * K,
         "setup_s": setup_s,
     }
     if dev_err:

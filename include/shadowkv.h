@@ -48,7 +48,14 @@ extern "C" {
 /* A CUDA stream (cudaStream_t) without pulling in the CUDA headers. */
 typedef struct CUstream_st* skv_stream;
 
-typedef enum { SKV_F32 = 0, SKV_BF16 = 1 } skv_dtype;
+/*
+ * SKV_FP8: the configuration the summary page's precision study runs with
+ * float8 e5m2 (section 5, "Precision sensitivity"): the landmarks the library
+ * builds and the values V (handed in as e5m2 bytes) are stored in e5m2; A, B,
+ * q, k_new, v_new, the keys and out stay bf16.  Scores stay bf16-exact (the
+ * query is split into three e5m2 terms for the 8-bit tensor-core product).
+ */
+typedef enum { SKV_F32 = 0, SKV_BF16 = 1, SKV_FP8 = 2 } skv_dtype;
 typedef enum { SKV_V_HBM = 0, SKV_V_HOST = 1 } skv_vplace;
 
 /*
@@ -72,7 +79,7 @@ typedef struct {
     int32_t max_new_tokens; /* decode steps the handle accepts */
     int64_t seq_len;        /* S */
     double  rope_base;      /* theta_i = rope_base^(-2i/d), half-split pairs (i, i+d/2) */
-    int32_t dtype;          /* skv_dtype: storage of A, B, V, q, keys, landmarks, out */
+    int32_t dtype;          /* skv_dtype: storage of A, B, V, q, keys, landmarks, out (SKV_FP8: see above) */
     int32_t v_place;        /* skv_vplace of V */
 } skv_config;
 

@@ -12,7 +12,8 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libshadowkv.so")
 
-SKV_F32, SKV_BF16 = 0, 1
+SKV_F32, SKV_BF16, SKV_FP8 = 0, 1, 2
+DTYPE_CODES = {"f32": SKV_F32, "bf16": SKV_BF16, "fp8": SKV_FP8}
 SKV_V_HBM, SKV_V_HOST = 0, 1
 PHASES = ("score", "select", "rebuild", "fetch", "attn")
 FIELDS = {
@@ -130,7 +131,7 @@ def make_config(w=None, **kw) -> SkvConfig:
                  head_dim=w.head_dim, rank=w.rank, chunk=w.chunk, n_select=w.n_select,
                  n_outlier=w.n_outlier, local_window=w.local_window, max_new_tokens=w.steps,
                  seq_len=w.seq_len, rope_base=w.rope_base,
-                 dtype=SKV_BF16 if w.dtype == "bf16" else SKV_F32,
+                 dtype=DTYPE_CODES[w.dtype],
                  v_place=SKV_V_HOST if w.v_place == "host" else SKV_V_HBM)
     f.update(kw)
     return SkvConfig(**f)

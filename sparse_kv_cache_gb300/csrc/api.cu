@@ -35,7 +35,9 @@ int fault_oom_at() {
     return 1;
 }
 
-int es_of(int dtype) { return dtype == SKV_BF16 ? 2 : 4; }
+int es_of(int dtype) { return dtype == SKV_F32 ? 4 : 2; }   // A, B, q, keys, out
+int es_l_of(int dtype) { return dtype == SKV_FP8 ? 1 : es_of(dtype); }   // landmarks
+int es_v_of(int dtype) { return dtype == SKV_FP8 ? 1 : es_of(dtype); }   // values
 
 }  // namespace
 
@@ -43,7 +45,8 @@ struct skv_layer {
     skv_config cfg{};
     int dev = 0, sm_count = 0;
     int U = 0, G = 0, H = 0, r = 0, K = 0, O = 0, W = 0, Tmax = 0, nchunk = 0, ncand = 0, n_c = 0;
-    int es = 0, dtype = 0, nkb = 0, loc_cap = 0, nhi = 0;
+    int es = 0, es_l = 0, es_v = 0, dtype = 0, nkb = 0, loc_cap = 0, nhi = 0;
+    bool tc = false;   // bf16 keys and factors: the tensor-core kernels
     int64_t S = 0;
     const void* A = nullptr;
     const void* B = nullptr;
@@ -75,6 +78,8 @@ struct skv_layer {
     CUtensorMap tmKall{};                 // the key blocks, [U*R][128], 128-row boxes (attention)
     int score_ncta = 0, score_nru = 0, score_nparts = 0, sel_smem_cap = 0;
     int32_t* sched = nullptr;
+    uint8_t* qt = nullptr;                // e5m2 scorer: the query's three terms, [U][3G][d]
+    float* qinv = nullptr;                // e5m2 scorer: 2^-s per head, [U][G]
     int64_t t = 0, t_reset = 0;
     cudaStream_t last_main = nullptr, last_side = nullptr;
     bool stepped = false;
@@ -137,6 +142,21 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+// 2-D byte tensor map (8-bit elements): rows of `cols` bytes, box = 128 bytes x box_rows,
+// 128-byte swizzle.
+int make_map_u8(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return SKV_ERR_CUDA;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols};
+    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SKV_OK : SKV_ERR_CUDA;
+}
+
 // 2-D bf16 tensor map: rows of `cols` elements, box = 64 columns x box_rows, 128-byte swizzle.
 int make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
     EncodeTiledFn enc = encode_fn();
@@ -171,14 +191,16 @@ int check_device_error(skv_layer* h) {
 // Algorithmic bytes of one decode step of one layer (every unit), given the
 // number of missed chunks summed over units.
 void step_bytes(const skv_config& c, int64_t t, double misses, double* hbm, double* link, double* scratch) {
-    const double es = es_of(c.dtype), d = c.head_dim, r = c.rank, C = c.chunk, K = c.n_select, O = c.n_outlier;
+    const double es = es_of(c.dtype), esl = es_l_of(c.dtype), esv = es_v_of(c.dtype);
+    const double d = c.head_dim, r = c.rank, C = c.chunk, K = c.n_select, O = c.n_outlier;
     const double U = static_cast<double>(c.batch) * c.n_kv_heads, G = c.n_q_heads / c.n_kv_heads;
     const double n_c = static_cast<double>(c.seq_len) / C - O - c.local_window / C;
     const double loc = c.local_window + t + 1;
-    double h = U * es * d * (2.0 * G + n_c + 2.0 * O * C + 2.0 * K * C + 2.0 * loc + 2.0);
-    h += misses * C * es * (r + 2.0 * d);       // A rows read, K and V rows written into slots
-    h += (misses > 0 ? U : 0.0) * es * r * d;   // B slices
-    double l = misses * C * d * es;             // value rows over the host link
+    // q and out, landmarks, the attended keys and values (outliers, cache, local), the append
+    double h = U * d * (es * 2.0 * G + esl * n_c + (es + esv) * (O * C + K * C + loc + 1.0));
+    h += misses * C * (es * r + es * d + esv * d);   // A rows read, K and V rows written into slots
+    h += (misses > 0 ? U : 0.0) * es * r * d;        // B slices
+    double l = misses * C * d * esv;                 // value rows over the host link
     if (c.v_place == SKV_V_HBM) { h += l; l = 0.0; }
     const double nsplit = std::ceil((O * C + K * C + loc) / attn_segment(c.dtype));
     *hbm = h;
@@ -224,7 +246,7 @@ int shadowkv_validate_config(const skv_config* c) {
     if (n_c < c->n_select) return SKV_ERR_INVALID;
     if (static_cast<int64_t>(c->batch) * c->seq_len > (int64_t(1) << 31) - 1) return SKV_ERR_INVALID;
     if (!(c->rope_base > 1.0) || !std::isfinite(c->rope_base)) return SKV_ERR_INVALID;
-    if (c->dtype != SKV_F32 && c->dtype != SKV_BF16) return SKV_ERR_INVALID;
+    if (c->dtype != SKV_F32 && c->dtype != SKV_BF16 && c->dtype != SKV_FP8) return SKV_ERR_INVALID;
     if (c->v_place != SKV_V_HBM && c->v_place != SKV_V_HOST) return SKV_ERR_INVALID;
     return SKV_OK;
 }
@@ -291,6 +313,9 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
     h->n_c = h->ncand - h->O;
     h->dtype = c.dtype;
     h->es = es_of(c.dtype);
+    h->es_l = es_l_of(c.dtype);
+    h->es_v = es_v_of(c.dtype);
+    h->tc = c.dtype != SKV_F32;
     h->nkb = (h->r + 63) / 64;
     h->loc_cap = h->W + h->Tmax;
     h->nhi = static_cast<int>((c.seq_len + 255) / 256);
@@ -328,7 +353,9 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
     }
 
     const int U = h->U, K = h->K, O = h->O, G = h->G, es = h->es;
-    const size_t row = static_cast<size_t>(kD) * es;
+    const size_t row = static_cast<size_t>(kD) * es;                 // a key (or bf16/fp32 value) row
+    const size_t row_l = static_cast<size_t>(kD) * h->es_l;           // a landmark row
+    const size_t row_v = static_cast<size_t>(kD) * h->es_v;           // a value row
     // scoring work: runs of kRunChunks landmarks of one unit; every CTA resident at once
     {
         h->score_nparts = score_parts(h->dtype);
@@ -340,11 +367,11 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
     h->sel_smem_cap = std::max(0, (200 * 1024 - 20 * K) / 4 - 4);
 
     const size_t nc = static_cast<size_t>(h->n_c);
-    if ((rc = alloc(h, &h->L, U * nc * row)) || (rc = alloc_t(h, &h->ids, U * nc)) ||
+    if ((rc = alloc(h, &h->L, U * nc * row_l)) || (rc = alloc_t(h, &h->ids, U * nc)) ||
         (rc = alloc_t(h, &h->out_ids, static_cast<size_t>(U) * std::max(O, 1))) ||
         (rc = alloc_t(h, &h->min_cos, static_cast<size_t>(U) * h->ncand)) ||
         (rc = alloc(h, &h->Kall, static_cast<size_t>(U) * (static_cast<size_t>(O + K) * kC + h->loc_cap) * row)) ||
-        (rc = alloc(h, &h->Vall, static_cast<size_t>(U) * (static_cast<size_t>(O + K) * kC + h->loc_cap) * row)) ||
+        (rc = alloc(h, &h->Vall, static_cast<size_t>(U) * (static_cast<size_t>(O + K) * kC + h->loc_cap) * row_v)) ||
         (rc = alloc_t(h, &h->sel_ids[0], static_cast<size_t>(U) * K)) ||
         (rc = alloc_t(h, &h->sel_ids[1], static_cast<size_t>(U) * K)) ||
         (rc = alloc_t(h, &h->sel_slot[0], static_cast<size_t>(U) * K)) ||
@@ -355,6 +382,8 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
         (rc = alloc_t(h, &h->logits, U * nc * G)) ||
         (rc = alloc_t(h, &h->score_part, static_cast<size_t>(U) * h->score_nru * h->score_nparts * G)) ||
         (rc = alloc_t(h, &h->sched, 1)) ||
+        (rc = alloc_t(h, &h->qt, static_cast<size_t>(U) * 3 * G * kD)) ||
+        (rc = alloc_t(h, &h->qinv, static_cast<size_t>(U) * G)) ||
         (rc = alloc_t(h, &h->vbuf, std::max(U * nc, static_cast<size_t>(U) * h->ncand))) ||
         (rc = alloc_t(h, &h->attn_cnt, static_cast<size_t>(U))) ||
         (rc = alloc_t(h, &h->rope_lo, static_cast<size_t>(256) * kD / 2)) ||
@@ -365,9 +394,9 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
     {
         uint8_t* kb = static_cast<uint8_t*>(h->Kall);
         uint8_t* vb = static_cast<uint8_t*>(h->Vall);
-        const size_t o_off = 0, c_off = static_cast<size_t>(O) * kC * row, l_off = static_cast<size_t>(O + K) * kC * row;
-        h->Kout = kb + o_off; h->Kc = kb + c_off; h->Kloc = kb + l_off;
-        h->Vout = vb + o_off; h->Vc = vb + c_off; h->Vloc = vb + l_off;
+        const size_t c_rows = static_cast<size_t>(O) * kC, l_rows = static_cast<size_t>(O + K) * kC;
+        h->Kout = kb; h->Kc = kb + c_rows * row; h->Kloc = kb + l_rows * row;
+        h->Vout = vb; h->Vc = vb + c_rows * row_v; h->Vloc = vb + l_rows * row_v;
     }
     {
         const int ntot_max = O * kC + K * kC + h->loc_cap;
@@ -377,7 +406,7 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
     }
     void* Lfull = nullptr;
     if ((rc = alloc(h, &Lfull, static_cast<size_t>(U) * h->ncand * kD * 4))) return fail(rc);
-    if (h->dtype == SKV_BF16 && (rc = alloc(h, &h->Bt, static_cast<size_t>(U) * h->r * kD * 2))) return fail(rc);
+    if (h->tc && (rc = alloc(h, &h->Bt, static_cast<size_t>(U) * h->r * kD * 2))) return fail(rc);
     if (cudaEventCreateWithFlags(&h->ev_sel, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&h->ev_fetch, cudaEventDisableTiming) != cudaSuccess)
         return fail(SKV_ERR_CUDA);
@@ -406,11 +435,12 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
     cudaMemsetAsync(h->hits_step, 0, h->Tmax * sizeof(int32_t), s);
     cudaMemsetAsync(h->miss_count, 0, U * sizeof(int32_t), s);
     cudaMemsetAsync(h->sched, 0, sizeof(int32_t), s);
-    if (h->dtype == SKV_BF16) {
+    if (h->tc) {
         if (launch_transpose_B(B, h->Bt, U, h->r, s)) return fail(SKV_ERR_CUDA);
         if ((rc = make_map(&h->tmA, A, h->r, static_cast<uint64_t>(c.batch) * c.seq_len, 8)) ||
             (rc = make_map(&h->tmB, h->Bt, h->r, static_cast<uint64_t>(U) * kD, 128)) ||
-            (rc = make_map(&h->tmL, h->L, kD, static_cast<uint64_t>(U) * h->n_c, kScTile)) ||
+            (rc = h->dtype == SKV_FP8 ? make_map_u8(&h->tmL, h->L, kD, static_cast<uint64_t>(U) * h->n_c, kScTile)
+                                      : make_map(&h->tmL, h->L, kD, static_cast<uint64_t>(U) * h->n_c, kScTile)) ||
             (rc = make_map(&h->tmKall, h->Kall, kD, static_cast<uint64_t>(U) * h->R, 128)))
             return fail(rc);
     }
@@ -423,7 +453,7 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
     auto rebuild = [&](const RebuildParams& p, int count_max) -> int {
         const int gx = (count_max + kTileChunks - 1) / kTileChunks;
         if (gx <= 0) return 0;
-        return h->dtype == SKV_BF16 ? launch_rebuild_tc(&h->tmA, &h->tmB, p, gx, s) : launch_rebuild_f32(p, gx, s);
+        return h->tc ? launch_rebuild_tc(&h->tmA, &h->tmB, p, gx, s) : launch_rebuild_f32(p, gx, s);
     };
     // 1. landmarks and min-cos of every candidate chunk (Algorithm 1: Reduce, CosineSimilarity, Min)
     {
@@ -463,7 +493,7 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
             if (rebuild(p, nloc)) return fail(SKV_ERR_CUDA);
         }
         GatherParams g{};
-        g.src = h->Vd; g.src_us = h->S * kD; g.nchunk = h->nchunk; g.es = es; g.U = U; g.err = h->err;
+        g.src = h->Vd; g.src_us = h->S * kD; g.nchunk = h->nchunk; g.es = h->es_v; g.U = U; g.err = h->err;
         if (O > 0) {
             GatherParams go = g;
             go.list = h->out_ids; go.list_us = O; go.list_cap = O; go.count_const = O; go.dst_cap = O;
@@ -512,6 +542,8 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     sp.L = h->L; sp.q = q; sp.logits = h->logits; sp.part = h->score_part; sp.n_c = h->n_c;
     sp.nru = h->score_nru; sp.total_runs = U * h->score_nru; sp.nparts = h->score_nparts; sp.sched = h->sched;
     sp.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(kD))); sp.err = h->err;
+    sp.qt = h->qt; sp.qinv = h->qinv;
+    if (h->dtype == SKV_FP8 && launch_qsplit(q, h->qt, h->qinv, U, G, sm)) return SKV_ERR_CUDA;
     if (launch_score(h->dtype, G, &h->tmL, sp, h->score_ncta, sm)) return SKV_ERR_CUDA;
     if (h->profiling) cudaEventRecord(ev[1], sm);
     // a3 + a4 + a1: top-K, index scan, append
@@ -524,7 +556,8 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     sel.cur_ids = h->sel_ids[(t + 1) & 1]; sel.cur_slot = h->sel_slot[(t + 1) & 1];
     sel.miss_chunk = h->miss_chunk; sel.miss_slot = h->miss_slot; sel.miss_count = h->miss_count;
     sel.hits_step = h->hits_step; sel.k_new = k_new; sel.v_new = v_new; sel.k_loc = h->Kloc; sel.v_loc = h->Vloc;
-    sel.loc_cap = h->loc_cap; sel.loc_pitch = h->R; sel.W = h->W; sel.es = h->es; sel.err = h->err;
+    sel.loc_cap = h->loc_cap; sel.loc_pitch = h->R; sel.W = h->W; sel.es = h->es; sel.es_v = h->es_v;
+    sel.err = h->err;
     if (launch_select_decode(h->dtype, sel, sm)) return SKV_ERR_CUDA;
     if (h->profiling) cudaEventRecord(ev[2], sm);
     // a6 on the side stream: value rows of the missed chunks into their slots
@@ -536,7 +569,7 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     GatherParams g{};
     g.src = h->Vd; g.src_us = h->S * kD; g.list = h->miss_chunk; g.list_us = K; g.list_cap = K;
     g.cnt = h->miss_count; g.dst_idx = h->miss_slot; g.dst_cap = K; g.dst = h->Vc;
-    g.dst_us = h->R * kD; g.nchunk = h->nchunk; g.es = h->es; g.U = U; g.err = h->err;
+    g.dst_us = h->R * kD; g.nchunk = h->nchunk; g.es = h->es_v; g.U = U; g.err = h->err;
     const int frc = launch_gather(g, (K + 7) / 8, ss);
     if (frc) return SKV_ERR_CUDA;
     if (h->profiling) cudaEventRecord(ev[6], ss);
@@ -548,7 +581,7 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     rp.dst_cap = K; rp.dst = h->Kc; rp.dst_us = h->R * kD;
     rp.rope_lo = h->rope_lo; rp.rope_hi = h->rope_hi; rp.nhi = h->nhi; rp.A = h->A; rp.B = h->B; rp.err = h->err;
     const int gx = (K + kTileChunks - 1) / kTileChunks;
-    const int rc = h->dtype == SKV_BF16 ? launch_rebuild_tc(&h->tmA, &h->tmB, rp, gx, sm) : launch_rebuild_f32(rp, gx, sm);
+    const int rc = h->tc ? launch_rebuild_tc(&h->tmA, &h->tmB, rp, gx, sm) : launch_rebuild_f32(rp, gx, sm);
     if (rc) return SKV_ERR_CUDA;
     if (h->profiling) cudaEventRecord(ev[3], sm);
     if (ss != sm) cudaStreamWaitEvent(sm, h->ev_fetch, 0);
@@ -562,7 +595,8 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     const int seg = attn_segment(h->dtype);
     ap.nsplit = (ap.n_out + ap.n_cache + ap.n_loc + seg - 1) / seg;
     ap.scale = sp.scale; ap.G = G; ap.U = U; ap.err = h->err;
-    if (h->dtype == SKV_BF16 ? launch_attn_tc(&h->tmKall, ap, h->sm_count, sm)
+    ap.v_es = h->es_v;
+    if (h->tc ? launch_attn_tc(&h->tmKall, ap, h->sm_count, sm)
                              : launch_attn(h->dtype, ap, sm))
         return SKV_ERR_CUDA;
     if (h->profiling) {
@@ -643,18 +677,18 @@ int shadowkv_reset_stats(skv_layer* h) {
 
 int64_t shadowkv_export_size(const skv_layer* h, int field) {
     if (!h) return -1;
-    const int64_t U = h->U, row = static_cast<int64_t>(kD) * h->es;
+    const int64_t U = h->U, row = static_cast<int64_t>(kD) * h->es, row_v = static_cast<int64_t>(kD) * h->es_v;
     switch (field) {
-        case SKV_F_LANDMARKS: return U * h->n_c * row;
+        case SKV_F_LANDMARKS: return U * h->n_c * kD * h->es_l;
         case SKV_F_CHUNK_IDS: return U * h->n_c * 4;
         case SKV_F_OUTLIER_IDS: return U * h->O * 4;
         case SKV_F_MIN_COS: return U * h->ncand * 4;
-        case SKV_F_K_OUTLIER:
-        case SKV_F_V_OUTLIER: return U * h->O * kC * row;
-        case SKV_F_K_LOCAL:
-        case SKV_F_V_LOCAL: return U * h->loc_cap * row;
-        case SKV_F_K_CACHE:
-        case SKV_F_V_CACHE: return U * h->K * kC * row;
+        case SKV_F_K_OUTLIER: return U * h->O * kC * row;
+        case SKV_F_V_OUTLIER: return U * h->O * kC * row_v;
+        case SKV_F_K_LOCAL: return U * h->loc_cap * row;
+        case SKV_F_V_LOCAL: return U * h->loc_cap * row_v;
+        case SKV_F_K_CACHE: return U * h->K * kC * row;
+        case SKV_F_V_CACHE: return U * h->K * kC * row_v;
         case SKV_F_SELECTION:
         case SKV_F_SLOT_OF_SEL: return U * h->K * 4;
         case SKV_F_MISS_COUNT: return U * 4;
@@ -693,7 +727,8 @@ int shadowkv_export(skv_layer* h, int field, void* dst, size_t bytes, skv_stream
         case SKV_F_K_CACHE: case SKV_F_V_CACHE: rows = static_cast<int64_t>(h->K) * kC; break;
     }
     if (rows > 0) {
-        const size_t rb = static_cast<size_t>(kD) * h->es;
+        const bool vfield = field == SKV_F_V_OUTLIER || field == SKV_F_V_LOCAL || field == SKV_F_V_CACHE;
+        const size_t rb = static_cast<size_t>(kD) * (vfield ? h->es_v : h->es);
         if (cudaMemcpy2DAsync(dst, rows * rb, src, h->R * rb, rows * rb, h->U, cudaMemcpyDefault, stream) != cudaSuccess) {
             cudaGetLastError();
             return SKV_ERR_CUDA;

@@ -430,7 +430,7 @@ __device__ __forceinline__ int acta_of(int f, int F, int ncta) {
 __device__ __forceinline__ void reader_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 __device__ __forceinline__ void value_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
-template <int G>
+template <int G, int VB>   // VB: bytes of a value element, 2 (bf16) or 1 (e5m2)
 __global__ void __launch_bounds__((kAWarps + 2) * 32, 1) k_attn_tc(const __grid_constant__ CUtensorMap tmK, AttnParams p) {
     constexpr int S = AStages<G>::value;
     extern __shared__ uint8_t smem_raw[];
@@ -499,11 +499,11 @@ __global__ void __launch_bounds__((kAWarps + 2) * 32, 1) k_attn_tc(const __grid_
                 // (rows past the unit's tokens are read but scored -inf; past the last block the
                 // copy fills zeros) and one bulk copy of the value rows
                 const int row = static_cast<int>(static_cast<int64_t>(ua) * p.unit_rows + seg0);
-                mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(kAKBytes + nseg * kD * 2));
+                mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(kAKBytes + nseg * kD * VB));
                 tma_load_2d_hint(sK, &tmK, 0, row, &full[st], pol);
                 tma_load_2d_hint(sK + 16384, &tmK, 64, row, &full[st], pol);
-                bulk_g2s_hint(sV, static_cast<const __nv_bfloat16*>(p.v_out) + (static_cast<int64_t>(ua) * p.unit_rows + seg0) * kD,
-                              static_cast<uint32_t>(nseg) * kD * 2, &full[st], pol);
+                bulk_g2s_hint(sV, static_cast<const uint8_t*>(p.v_out) + (static_cast<int64_t>(ua) * p.unit_rows + seg0) * kD * VB,
+                              static_cast<uint32_t>(nseg) * kD * VB, &full[st], pol);
             }
             // the unit's query rows g < G (the MMA's other columns are never read), written while
             // the copies are in flight; the second arrival publishes them
@@ -691,7 +691,8 @@ __global__ void __launch_bounds__((kAWarps + 2) * 32, 1) k_attn_tc(const __grid_
 #pragma unroll 4
             for (int r = hw; r < nseg; r += 8) {
                 float v[8];
-                load8(reinterpret_cast<const __nv_bfloat16*>(sV + r * kD * 2) + hl * 8, v);
+                if constexpr (VB == 1) load8_e5m2(sV + r * kD + hl * 8, v);
+                else load8(reinterpret_cast<const __nv_bfloat16*>(sV + r * kD * 2) + hl * 8, v);
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
                     const float pg = sP[buf][r * G + g];
@@ -769,25 +770,25 @@ __global__ void __launch_bounds__(kD) k_attn_merge(AttnParams p, int ncta) {
         static_cast<__nv_bfloat16*>(p.out)[(static_cast<int64_t>(u) * G + g) * kD + dim] = __float2bfloat16_rn(A[g] / L[g]);
 }
 
-template <int G>
+template <int G, int VB>
 static int launch_tc(const CUtensorMap* tmK, const AttnParams& p, int nsm, cudaStream_t s) {
     const int ntot = p.n_out + p.n_cache + p.n_loc;
     if (!tmK || p.nsplit != (ntot + kBSeg - 1) / kBSeg || nsm <= 0) return -1;
     // the block layout, regions adjacent in each block
-    const size_t rb = static_cast<size_t>(kD) * 2;
+    const size_t rb = static_cast<size_t>(kD) * 2, rbv = static_cast<size_t>(kD) * VB;
     if (p.unit_rows < static_cast<int64_t>(p.n_out) + p.n_cache + p.n_loc ||
         static_cast<const uint8_t*>(p.k_c) != static_cast<const uint8_t*>(p.k_out) + p.n_out * rb ||
         static_cast<const uint8_t*>(p.k_loc) != static_cast<const uint8_t*>(p.k_c) + static_cast<size_t>(p.n_cache) * rb ||
-        static_cast<const uint8_t*>(p.v_c) != static_cast<const uint8_t*>(p.v_out) + p.n_out * rb ||
-        static_cast<const uint8_t*>(p.v_loc) != static_cast<const uint8_t*>(p.v_c) + static_cast<size_t>(p.n_cache) * rb)
+        static_cast<const uint8_t*>(p.v_c) != static_cast<const uint8_t*>(p.v_out) + p.n_out * rbv ||
+        static_cast<const uint8_t*>(p.v_loc) != static_cast<const uint8_t*>(p.v_c) + static_cast<size_t>(p.n_cache) * rbv)
         return -1;
     const int64_t F = static_cast<int64_t>(p.U) * p.nsplit;
     const int ncta = static_cast<int>(F < nsm ? F : nsm);
     if (ncta <= 0) return 0;
     if (F * (ncta + 1) > INT32_MAX || static_cast<int64_t>(p.U) * p.unit_rows > INT32_MAX) return -1;   // 32-bit indexing
     const size_t smem = static_cast<size_t>(AStages<G>::value) * kAStage + static_cast<size_t>(4) * G * kD * 4 + 1024;
-    cudaFuncSetAttribute(k_attn_tc<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    k_attn_tc<G><<<ncta, (kAWarps + 2) * 32, smem, s>>>(*tmK, p);
+    cudaFuncSetAttribute(k_attn_tc<G, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    k_attn_tc<G, VB><<<ncta, (kAWarps + 2) * 32, smem, s>>>(*tmK, p);
     if (cudaGetLastError() != cudaSuccess) return -1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.U);
@@ -808,15 +809,15 @@ static int launch_tc(const CUtensorMap* tmK, const AttnParams& p, int nsm, cudaS
 
 int launch_attn_tc(const CUtensorMap* k_all, const AttnParams& p, int nsm, cudaStream_t s) {
     switch (p.G) {
-        case 1: return launch_tc<1>(k_all, p, nsm, s);
-        case 2: return launch_tc<2>(k_all, p, nsm, s);
-        case 4: return launch_tc<4>(k_all, p, nsm, s);
-        case 8: return launch_tc<8>(k_all, p, nsm, s);
+        case 1: return p.v_es == 1 ? launch_tc<1, 1>(k_all, p, nsm, s) : launch_tc<1, 2>(k_all, p, nsm, s);
+        case 2: return p.v_es == 1 ? launch_tc<2, 1>(k_all, p, nsm, s) : launch_tc<2, 2>(k_all, p, nsm, s);
+        case 4: return p.v_es == 1 ? launch_tc<4, 1>(k_all, p, nsm, s) : launch_tc<4, 2>(k_all, p, nsm, s);
+        case 8: return p.v_es == 1 ? launch_tc<8, 1>(k_all, p, nsm, s) : launch_tc<8, 2>(k_all, p, nsm, s);
     }
     return -1;
 }
 
-int attn_segment(int dtype) { return dtype == 1 ? kBSeg : kAttnSeg; }
+int attn_segment(int dtype) { return dtype != 0 ? kBSeg : kAttnSeg; }
 
 template <typename T, int G>
 static int launch_t(const AttnParams& p, cudaStream_t s) {

@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(256) k_compact(CompactParams p) {
 int launch_compact(const CompactParams& p, cudaStream_t s) {
     const dim3 grid(static_cast<unsigned>((p.ncand + 7) / 8), p.U);
     if (p.dtype == 1) k_compact<__nv_bfloat16><<<grid, 256, 0, s>>>(p);
+    else if (p.dtype == 2) k_compact<__nv_fp8_e5m2><<<grid, 256, 0, s>>>(p);   // e5m2 landmarks
     else k_compact<float><<<grid, 256, 0, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }

@@ -389,6 +389,309 @@ __global__ void __launch_bounds__(192, 1) k_score_tc(const __grid_constant__ CUt
     }
 }
 
+// ------------------------------------------------------------------ e5m2 landmarks (fp8 configuration)
+// The same persistent pipeline over landmarks stored in e5m2: 256 landmarks per stage (two
+// 128 x 128-byte TMA boxes, two M = 128 MMA halves) and kind::f8f6f4 MMAs (K = 32 per
+// instruction).  The bf16 query enters as three e5m2
+// terms per head, t1 = e5m2(x), t2 = e5m2(x - t1), t3 = e5m2(x - t1 - t2) of x = q * 2^s
+// with 2^s the largest power of two keeping max|x| <= 2^14: each term carries the next three
+// significant bits, so t1 + t2 + t3 = x exactly for every component down to max|q| * 2^-22,
+// and the epilogue's (col_g + col_{G+g} + col_{2G+g}) * 2^-s is the bf16-query score.
+struct ScTile8 {
+    int run, nv;
+    int64_t j;
+    int unit, last;
+    float inv[8];   // 2^-s of each head's query
+};
+
+template <int G>
+__global__ void __launch_bounds__(192, 1) k_score_f8(const __grid_constant__ CUtensorMap tmL, ScoreParams p) {
+    constexpr int NQ = (3 * G <= 16) ? 16 : 32;   // MMA N: the 3G term rows, padded
+    constexpr int kQBytes = NQ * 128;
+    constexpr int kT8 = 2 * kScTile;              // 256 landmarks per stage: two M = 128 halves
+    constexpr int kStage = 32768 + kQBytes;
+    constexpr int S = kScStages8;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ uint64_t full[S], empty[S], accf[2], acce[2], drain;
+    __shared__ ScTile8 stile[S], atile[2];
+    __shared__ uint32_t tmem_slot;
+    __shared__ volatile int s_abort;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t n_c = p.n_c;
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        for (int b = 0; b < 2; ++b) { mbar_init(&accf[b], 2); mbar_init(&acce[b], 4); }
+        mbar_init(&drain, 1);
+        s_abort = 0;
+        fence_mbar_init();
+        prefetch_tensormap(&tmL);
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_slot, 4 * NQ);   // 2 buffers x 2 halves
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    pdl_wait();
+    pdl_trigger();
+
+    if (warp == 0) {
+        // ------------------------------------------------ producer warp
+        const uint64_t pol = l2_evict_first();   // read once per step
+        int it = 0;
+        int next = (lane == 0) ? atomicAdd(p.sched, 1) : 0;
+        next = __shfl_sync(0xffffffffu, next, 0);
+        bool done = false;
+        while (!done) {
+            const int r = s_abort ? p.total_runs : next;
+            int64_t a = 0, e = 0;
+            int u = 0;
+            if (r < p.total_runs) {
+                u = r / p.nru;
+                a = static_cast<int64_t>(u) * n_c + static_cast<int64_t>(r % p.nru) * kRunChunks;
+                e = min(a + kRunChunks, static_cast<int64_t>(u + 1) * n_c);
+                int nx = (lane == 0) ? atomicAdd(p.sched, 1) : 0;   // claim the next run early
+                next = __shfl_sync(0xffffffffu, nx, 0);
+            } else {
+                done = true;
+            }
+            // the run's query terms (formed once per step by k_qsplit): rows n = jt*G + g of
+            // [3G][128 B]; lane l holds 16-byte words l, l + 32, ... and the heads' 2^-s
+            constexpr int QW8 = (3 * G * 8 + 31) / 32;
+            uint4 tq[QW8];
+#pragma unroll
+            for (int w = 0; w < QW8; ++w) {
+                const int word = lane + 32 * w;
+                tq[w] = make_uint4(0, 0, 0, 0);
+                if (!done && word < 3 * G * 8) tq[w] = reinterpret_cast<const uint4*>(p.qt + static_cast<int64_t>(u) * 3 * G * 128)[word];
+            }
+            float inv[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) inv[g] = done ? 0.f : p.qinv[u * G + g];
+            for (int64_t j = a; done || j < e; j += kT8, ++it) {
+                const int s = it % S;
+                uint8_t* st = smem + s * kStage;
+                const int okw = mbar_wait(&empty[s], ((it / S) & 1) ^ 1) ? 1 : 0;
+                if (!__all_sync(0xffffffffu, okw)) {
+                    if (lane == 0) set_err(p.err, DEV_ERR_TIMEOUT, 131);
+                    s_abort = 1;
+                    done = true;
+                }
+                if (done) {   // end marker: a plain arrival completes the stage's phase
+                    if (lane == 0) {
+                        stile[s].run = -1;
+                        mbar_arrive(&full[s]);
+                    }
+                    ++it;
+                    break;
+                }
+                // term rows of the [NQ rows][128 B] swizzled query tile
+                uint8_t* sq = st + 32768;
+#pragma unroll
+                for (int w = 0; w < QW8; ++w) {
+                    const int word = lane + 32 * w, n = word >> 3, c = word & 7;
+                    if (word < 3 * G * 8)
+                        *reinterpret_cast<uint4*>(sq + (n >> 3) * 1024 + (n & 7) * 128 + ((c ^ (n & 7)) << 4)) = tq[w];
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    ScTile8 t;
+                    t.run = r;
+                    t.j = j;
+                    t.nv = static_cast<int>(min(static_cast<int64_t>(kT8), e - j));
+                    t.unit = u;
+                    t.last = (j + kT8 >= e);
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) t.inv[g] = g < G ? inv[g] : 0.f;
+                    stile[s] = t;
+                    // rows past the tensor's end read as zeros; rows past the run are never scored
+                    mbar_arrive_expect_tx(&full[s], 32768);
+                    tma_load_2d_hint(st, &tmL, 0, static_cast<int>(j), &full[s], pol);
+                    tma_load_2d_hint(st + 16384, &tmL, 0, static_cast<int>(j + kScTile), &full[s], pol);
+                }
+                __syncwarp();
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        constexpr uint32_t idesc = idesc_e5m2_f32(kScTile, NQ);
+        int it = 0;
+        while (true) {
+            const int s = it % S, b = it & 1;
+            int ok = mbar_wait(&full[s], (it / S) & 1) ? 1 : 0;
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) { if (lane == 0) set_err(p.err, DEV_ERR_TIMEOUT, 132); s_abort = 1; break; }
+            const ScTile8 t = stile[s];
+            if (lane == 0) ok = mbar_wait(&acce[b], ((it >> 1) & 1) ^ 1) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) { if (lane == 0) set_err(p.err, DEV_ERR_TIMEOUT, 133); s_abort = 1; break; }
+            if (t.run < 0) {
+                if (lane == 0) { atile[b] = t; mbar_arrive_cnt(&accf[b], 2); }
+                break;
+            }
+            if (lane == 0) {
+                tc_fence_after();
+                const uint8_t* st = smem + s * kStage;
+                for (int h = 0; h < 2; ++h)
+                    for (int k = 0; k < 4; ++k) {   // K = 128 bytes = 4 x 32 e5m2 values
+                        const uint64_t ad = smem_desc_sw128(smem_u32(st + h * 16384 + k * 32));
+                        const uint64_t bd = smem_desc_sw128(smem_u32(st + 32768 + k * 32));
+                        tc_mma_f8(tmem + (2 * b + h) * NQ, ad, bd, idesc, k > 0 ? 1u : 0u);
+                    }
+                tc_commit(&empty[s]);
+                tc_commit(&accf[b]);
+                atile[b] = t;
+                mbar_arrive(&accf[b]);   // release: the record is visible once the phase completes
+            }
+            __syncwarp();
+            ++it;
+        }
+        if (lane == 0) tc_commit(&drain);
+        __syncwarp();
+        (void)mbar_wait(&drain, 0);
+    } else {
+        // ------------------------------------------------ epilogue: 4 warps, one landmark row per thread
+        const int quarter = warp & 3;                     // TMEM lanes [32*quarter, +32)
+        const int row = quarter * 32 + lane;
+        const int ew = warp - 2;
+        float m[G], sx[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) { m[g] = -CUDART_INF_F; sx[g] = 0.f; }
+        for (int it = 0;; ++it) {
+            const int b = it & 1;
+            if (!mbar_wait(&accf[b], (it >> 1) & 1)) {
+                set_err(p.err, DEV_ERR_TIMEOUT, 135);
+                s_abort = 1;
+                break;
+            }
+            const ScTile8 t = atile[b];
+            if (t.run < 0) break;
+            tc_fence_after();
+            constexpr int NC8 = (3 * G + 7) / 8;
+            float v[2][NC8 * 8];
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int c8 = 0; c8 < NC8; ++c8) {
+                    float w[8];
+                    tmem_ld8(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + (2 * b + h) * NQ + 8 * c8, w);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) v[h][8 * c8 + kk] = w[kk];
+                }
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acce[b]);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int rr = h * kScTile + row;
+                if (rr >= t.nv) continue;
+                float z[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) z[g] = (v[h][g] + v[h][G + g] + v[h][2 * G + g]) * t.inv[g] * p.scale;
+                float* dst = p.logits + (t.j + rr) * G;
+                if constexpr (G == 4) {
+                    *reinterpret_cast<float4*>(dst) = make_float4(z[0], z[1], z[2], z[3]);
+                } else {
+#pragma unroll
+                    for (int g = 0; g < G; ++g) dst[g] = z[g];
+                }
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    if (z[g] > m[g]) {
+                        sx[g] = sx[g] * __expf(m[g] - z[g]) + 1.f;
+                        m[g] = z[g];
+                    } else {
+                        sx[g] += __expf(z[g] - m[g]);
+                    }
+                }
+            }
+            if (t.last) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float M = warp_max(m[g]);
+                    const float tt = (m[g] == -CUDART_INF_F) ? 0.f : sx[g] * __expf(m[g] - M);
+                    const float Ssum = warp_sum(tt);
+                    if (lane == 0) p.part[(static_cast<int64_t>(t.run) * kScParts + ew) * G + g] = make_float2(M, Ssum);
+                    m[g] = -CUDART_INF_F;
+                    sx[g] = 0.f;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 4 * NQ);
+    }
+}
+
+// The query terms of the e5m2 scorer, once per step: block u, thread = dimension; per head
+// the largest |q| over the 128 dimensions sets 2^s (largest power of two with
+// max|q| * 2^s < 2^14), then x = q * 2^s gives t1 = e5m2(x), t2 = e5m2(x - t1),
+// t3 = e5m2(x - t1 - t2) into rows jt*G + g of qt[u], and qinv[u][g] = 2^-s.
+template <int G>
+__global__ void __launch_bounds__(kD) k_qsplit(const __nv_bfloat16* __restrict__ q, uint8_t* __restrict__ qt,
+                                               float* __restrict__ qinv) {
+    __shared__ float red[4];
+    const int u = blockIdx.x, dim = threadIdx.x, lane = dim & 31, warp = dim >> 5;
+#pragma unroll 1
+    for (int g = 0; g < G; ++g) {
+        const float x0 = __bfloat162float(q[(static_cast<int64_t>(u) * G + g) * kD + dim]);
+        float mx = warp_max(fabsf(x0));
+        if (lane == 0) red[warp] = mx;
+        __syncthreads();
+        mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+        __syncthreads();
+        int sh = 0;
+        if (mx > 0.f) {
+            int ex;
+            frexpf(mx, &ex);               // mx in [2^(ex-1), 2^ex)
+            sh = max(-100, min(100, 14 - ex));
+        }
+        float r = x0 * ldexpf(1.f, sh);
+        uint8_t* row = qt + static_cast<int64_t>(u) * 3 * G * kD;
+#pragma unroll
+        for (int jt = 0; jt < 3; ++jt) {
+            const uint32_t b8 = from_f<__nv_fp8_e5m2>(r).__x;
+            row[(jt * G + g) * kD + dim] = static_cast<uint8_t>(b8);
+            r -= e5m2_to_f(b8);
+        }
+        if (dim == 0) qinv[u * G + g] = ldexpf(1.f, -sh);
+    }
+}
+
+int launch_qsplit(const void* q, void* qt, float* qinv, int U, int G, cudaStream_t s) {
+    auto q16 = static_cast<const __nv_bfloat16*>(q);
+    auto qt8 = static_cast<uint8_t*>(qt);
+    switch (G) {
+        case 1: k_qsplit<1><<<U, kD, 0, s>>>(q16, qt8, qinv); break;
+        case 2: k_qsplit<2><<<U, kD, 0, s>>>(q16, qt8, qinv); break;
+        case 4: k_qsplit<4><<<U, kD, 0, s>>>(q16, qt8, qinv); break;
+        case 8: k_qsplit<8><<<U, kD, 0, s>>>(q16, qt8, qinv); break;
+        default: return -1;
+    }
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+template <int G>
+static int launch_f8(const CUtensorMap* tmL, const ScoreParams& p, int ncta, cudaStream_t s) {
+    constexpr int NQ = (3 * G <= 16) ? 16 : 32;
+    const int smem = kScStages8 * (32768 + NQ * 128) + 1024;
+    cudaFuncSetAttribute(k_score_f8<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (launch_pdl(k_score_f8<G>, dim3(ncta), dim3(192), smem, s, *tmL, p) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    return 0;
+}
+
 template <int G>
 static int launch_tc(const CUtensorMap* tmL, const ScoreParams& p, int ncta, cudaStream_t s) {
     const int smem = kScStages * (32768 + 4096) + 1024;
@@ -429,6 +732,11 @@ static int occ_t() {
     }
 
 int launch_score(int dtype, int G, const CUtensorMap* tmL, const ScoreParams& p, int ncta, cudaStream_t s) {
+    if (dtype == 2) {
+#define CALL8(g) launch_f8<g>(tmL, p, ncta, s)
+        SKV_G_DISPATCH(G, CALL8)
+#undef CALL8
+    }
     if (dtype == 1) {
 #define CALLB(g) launch_tc<g>(tmL, p, ncta, s)
         SKV_G_DISPATCH(G, CALLB)
@@ -440,12 +748,12 @@ int launch_score(int dtype, int G, const CUtensorMap* tmL, const ScoreParams& p,
     }
 }
 
-int score_parts(int dtype) { return dtype == 1 ? kScParts : kScoreWarps; }
+int score_parts(int dtype) { return dtype != 0 ? kScParts : kScoreWarps; }
 
 int score_ctas_per_sm(int dtype, int G) {
-    if (dtype == 1) {
+    if (dtype != 0) {
         (void)G;
-        return 1;   // the tensor-core kernel holds 217 KB of shared memory
+        return 1;   // the tensor-core kernels hold most of the shared memory
     } else {
 #define OCCF(g) occ_t<float, g>()
         SKV_G_DISPATCH(G, OCCF)

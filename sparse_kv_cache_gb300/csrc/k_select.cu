@@ -273,11 +273,28 @@ __global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
         if (row < p.loc_cap) {
             const int64_t off = (static_cast<int64_t>(u) * p.loc_pitch + row) * kD * p.es;
             const int64_t src = static_cast<int64_t>(u) * kD * p.es;
-            if (wt < n16)
+            if (wt < n16) {
                 copy_row16(static_cast<uint8_t*>(p.k_loc) + off, static_cast<const uint8_t*>(p.k_new) + src, n16, wt, 1 << 30);
-            else if (wt >= 64 && wt < 64 + n16)
+            } else if (p.es_v == 1) {
+                // e5m2 value storage: 16 threads round 8 bf16 values each
+                const int vt = wt - 64;
+                if (vt >= 0 && vt < kD / 8) {
+                    const __nv_bfloat16* vs = static_cast<const __nv_bfloat16*>(p.v_new) + static_cast<int64_t>(u) * kD + vt * 8;
+                    uint8_t* vd = static_cast<uint8_t*>(p.v_loc) + (static_cast<int64_t>(u) * p.loc_pitch + row) * kD + vt * 8;
+                    float f[8];
+                    load8(vs, f);
+                    uint32_t lo = 0, hi = 0;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        lo |= static_cast<uint32_t>(from_f<__nv_fp8_e5m2>(f[i]).__x) << (8 * i);
+                        hi |= static_cast<uint32_t>(from_f<__nv_fp8_e5m2>(f[4 + i]).__x) << (8 * i);
+                    }
+                    *reinterpret_cast<uint2*>(vd) = make_uint2(lo, hi);
+                }
+            } else if (wt >= 64 && wt < 64 + n16) {
                 copy_row16(static_cast<uint8_t*>(p.v_loc) + off, static_cast<const uint8_t*>(p.v_new) + src, n16, wt - 64,
                            1 << 30);
+            }
         } else if (wt == 0) {
             set_err(p.err, DEV_ERR_BOUNDS, 316);
         }

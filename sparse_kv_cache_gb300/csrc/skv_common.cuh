@@ -6,6 +6,8 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -78,6 +80,26 @@ template <typename T> __device__ __forceinline__ T from_f(float x);
 template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
     return __float2bfloat16_rn(x);
+}
+// e5m2 (1 sign, 5 exponent bits with bias 15, 2 mantissa bits), nearest even, saturating
+template <> __device__ __forceinline__ __nv_fp8_e5m2 from_f<__nv_fp8_e5m2>(float x) {
+    __nv_fp8_e5m2 r;
+    r.__x = __nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E5M2);
+    return r;
+}
+// An e5m2 byte is the upper byte of the binary16 value with the same sign, exponent
+// (same width and bias) and leading mantissa bits, so decoding is a shift.
+__device__ __forceinline__ float e5m2_to_f(uint32_t byte) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(byte << 8)));
+}
+// 8 consecutive e5m2 values (8-byte aligned) as fp32
+__device__ __forceinline__ void load8_e5m2(const uint8_t* p, float (&v)[8]) {
+    const uint2 w = *reinterpret_cast<const uint2*>(p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[i] = e5m2_to_f((w.x >> (8 * i)) & 0xFF);
+        v[4 + i] = e5m2_to_f((w.y >> (8 * i)) & 0xFF);
+    }
 }
 
 // Copy one row of `n16` 16-byte words (any dtype) with 16-byte loads, lane-strided.
@@ -233,6 +255,16 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, ui
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// D (+)= A . B^T with 8-bit float operands (kind::f8f6f4; the instruction descriptor's A/B
+// format fields select e4m3 = 0 or e5m2 = 1), fp32 accumulator; K = 32 per instruction.
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // Arrive on `bar` once every tcgen05.mma issued so far by this thread has completed.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -281,6 +313,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
     return (1u << 4)                                  // D format: f32
            | (1u << 7)                                // A format: bf16
            | (1u << 10)                               // B format: bf16
+           | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+
+// Instruction descriptor of kind::f8f6f4 with e5m2 A and B, fp32 D (K-major A and B).
+__host__ __device__ constexpr uint32_t idesc_e5m2_f32(int M, int N) {
+    return (1u << 4)                                  // D format: f32
+           | (1u << 7)                                // A format: e5m2
+           | (1u << 10)                               // B format: e5m2
            | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
 }

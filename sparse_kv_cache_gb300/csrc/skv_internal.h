@@ -23,12 +23,14 @@ enum : int { DEV_ERR_BOUNDS = 1, DEV_ERR_TIMEOUT = 2, DEV_ERR_NUMERIC = 3 };
 // tensor-core scoring (bf16): 128-chunk tiles, 6-stage TMA ring, 4 epilogue warps
 constexpr int kScTile = 128;
 constexpr int kScStages = 6;
+constexpr int kScStages8 = 6;   // e5m2 scorer: 2 x 16 KB tiles + query terms per stage
 constexpr int kScN = 16;          // MMA N: the G <= 8 query heads, zero-padded
 constexpr int kScParts = 4;       // partial records per (CTA, unit): one per epilogue warp
 
 constexpr int kRunChunks = 512;   // landmarks per unit of scheduled scoring work
 
 struct ScoreParams {
+    const uint8_t* qt; const float* qinv;   // e5m2 scorer: query terms [U][3G][d], 2^-s [U][G]
     const void* L;        // [U][n_c][d]
     const void* q;        // [U*G][d]
     float* logits;        // [U][n_c][G]  z = q.L / sqrt(d)
@@ -43,6 +45,7 @@ struct ScoreParams {
 };
 // bf16: tcgen05 kernel through the tensor map of L; fp32: CUDA-core kernel
 int launch_score(int dtype, int G, const CUtensorMap* tmL, const ScoreParams& p, int ncta, cudaStream_t s);
+int launch_qsplit(const void* q, void* qt, float* qinv, int U, int G, cudaStream_t s);   // e5m2 query terms
 int score_ctas_per_sm(int dtype, int G);
 int score_parts(int dtype);
 
@@ -73,6 +76,7 @@ struct SelectParams {
     // append of the new token
     const void* k_new; const void* v_new; void* k_loc; void* v_loc;
     int loc_cap; int64_t loc_pitch; int W; int es;   // local rows of unit u start at u * loc_pitch
+    int es_v;             // bytes of a value element: 1 stores the new value in e5m2
     int* err;
 };
 int launch_select_decode(int dtype, const SelectParams& p, cudaStream_t s);
@@ -132,6 +136,7 @@ struct AttnParams {
     // > 0: the three regions are slices of per-unit blocks of unit_rows rows (unit u's rows of
     // every region start at base + u * unit_rows); 0: each region is packed [U][its rows][d]
     int64_t unit_rows;
+    int v_es;                      // bytes of a value element: 2 (bf16) or 1 (e5m2; tensor-core form only)
     void* out;                     // [U*G][d]
     float* part;                   // [U][nsplit][G][d + 4]
     int* counter;                  // [U]

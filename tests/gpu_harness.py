@@ -20,6 +20,12 @@ def np64(t: torch.Tensor) -> np.ndarray:
     return t.detach().to("cpu").double().numpy()
 
 
+def e5m2_ulp(x: np.ndarray) -> np.ndarray:
+    """Spacing of e5m2 values at |x|: 2^(e-2) in [2^e, 2^(e+1)), 2^-16 below 2^-14."""
+    a = np.maximum(np.abs(x), 2.0 ** -14)
+    return 2.0 ** (np.floor(np.log2(a)) - 2)
+
+
 def bf16_ulp(x: np.ndarray) -> np.ndarray:
     """Spacing of bfloat16 numbers at |x| (8 significant bits)."""
     ax = np.maximum(np.abs(x), 2.0 ** -126)
@@ -84,7 +90,12 @@ class LayerRun:
         return buf.view(*shape)
 
     def sdtype(self):
-        return torch.bfloat16 if self.w.dtype == "bf16" else torch.float32
+        """Storage of the keys (and, except in the fp8 configuration, of landmarks and values)."""
+        return torch.float32 if self.w.dtype == "f32" else torch.bfloat16
+
+    def vdtype(self):
+        """Storage of the values and the landmarks."""
+        return torch.float8_e5m2 if self.w.dtype == "fp8" else self.sdtype()
 
     # ------------------------------------------------------------ oracle per unit
     def unit_inputs(self, u: int):
@@ -116,15 +127,16 @@ def check_prefill(run: LayerRun, units) -> dict:
     w = run.w
     U, O, C, W, d = w.units, w.n_outlier, w.chunk, w.local_window, w.head_dim
     ncand = w.n_chunks - W // C
-    sd = run.sdtype()
-    L_t = run.export("landmarks", sd, (U, w.n_selectable, d))
+    sd, vd = run.sdtype(), run.vdtype()
+    kd = ref.key_storage(w.dtype)
+    L_t = run.export("landmarks", vd, (U, w.n_selectable, d))
     ids_t = run.export("chunk_ids", torch.int32, (U, w.n_selectable))
     oid = run.export("outlier_ids", torch.int32, (U, O)).cpu().numpy() if O else np.zeros((U, 0), int)
     mcos_t = run.export("min_cos", torch.float32, (U, ncand))
     kout_t = run.export("k_outlier", sd, (U, O * C, d)) if O else None
-    vout_t = run.export("v_outlier", sd, (U, O * C, d)) if O else None
+    vout_t = run.export("v_outlier", vd, (U, O * C, d)) if O else None
     kloc_t = run.export("k_local", sd, (U, W + run.steps, d))
-    vloc_t = run.export("v_local", sd, (U, W + run.steps, d))
+    vloc_t = run.export("v_local", vd, (U, W + run.steps, d))
     ties = 0
     for u in units:
         pre = run.oracle_prefill(u)
@@ -150,17 +162,20 @@ def check_prefill(run: LayerRun, units) -> dict:
         Lo = pre.all_landmarks[ids[u]]
         if w.dtype == "bf16":
             _within(L[u], ref.bf16_round(Lo), bf16_ulp(Lo) + FP32_ABS, "landmarks (bf16)")
+        elif w.dtype == "fp8":
+            # the GPU rounds its fp32 mean, the oracle its float64 mean: one e5m2 step apart at most
+            _within(L[u], ref.e5m2_round(Lo), e5m2_ulp(Lo) + FP32_ABS, "landmarks (e5m2)")
         else:
             _within(L[u], Lo, 2e-5, "landmarks (fp32)")
         # outlier chunks' keys and values
         if O:
             tok = ref.chunk_tokens(oid[u], C)
             Ko = ref.rebuild_keys(A[tok], B, tok, w.rope_base)
-            _close_keys(kout[u], Ko, w.dtype, "k_outlier")
+            _close_keys(kout[u], Ko, kd, "k_outlier")
             assert np.array_equal(vout[u], V[tok]), "v_outlier"
         # local window
         Kl = ref.rebuild_keys(A[w.seq_len - W:], B, np.arange(w.seq_len - W, w.seq_len), w.rope_base)
-        _close_keys(kloc[u][:W], Kl, w.dtype, "k_local")
+        _close_keys(kloc[u][:W], Kl, kd, "k_local")
         assert np.array_equal(vloc[u][:W], V[w.seq_len - W:]), "v_local"
     return {"outlier_near_ties": ties}
 
@@ -195,8 +210,9 @@ def check_step(run: LayerRun, units, rep: Report, prev_sel: dict, check_cache: b
     w = run.w
     t = run.t - 1
     U, G, K, C, d, W = w.units, w.group, w.n_select, w.chunk, w.head_dim, w.local_window
-    sd = run.sdtype()
-    L_t = run.export("landmarks", sd, (U, w.n_selectable, d))
+    sd, vd = run.sdtype(), run.vdtype()
+    kd = ref.key_storage(w.dtype)
+    L_t = run.export("landmarks", vd, (U, w.n_selectable, d))
     ids_t = run.export("chunk_ids", torch.int32, (U, w.n_selectable))
     oid = run.export("outlier_ids", torch.int32, (U, w.n_outlier)).cpu().numpy() if w.n_outlier else None
     sel = run.sel.view(U, K).cpu().numpy()
@@ -209,7 +225,7 @@ def check_step(run: LayerRun, units, rep: Report, prev_sel: dict, check_cache: b
     kc_t = vc_t = None
     if check_cache:
         kc_t = run.export("k_cache", sd, (U, K * C, d))
-        vc_t = run.export("v_cache", sd, (U, K * C, d))
+        vc_t = run.export("v_cache", vd, (U, K * C, d))
     for u in units:
         pre = run.oracle_prefill(u)
         _, A, B, V = run._pre[u]
@@ -234,7 +250,7 @@ def check_step(run: LayerRun, units, rep: Report, prev_sel: dict, check_cache: b
             for i in range(K):
                 ch, s = int(sel[u][i]), int(slots[u][i])
                 tok = ref.chunk_tokens([ch], C)
-                _close_keys(kc[u][s * C:(s + 1) * C], ref.rebuild_keys(A[tok], B, tok, w.rope_base), w.dtype,
+                _close_keys(kc[u][s * C:(s + 1) * C], ref.rebuild_keys(A[tok], B, tok, w.rope_base), kd,
                             "k_cache")
                 assert np.array_equal(vc[u][s * C:(s + 1) * C], V[tok]), "v_cache"
         # output = exact attention over the GPU's index set
@@ -242,14 +258,15 @@ def check_step(run: LayerRun, units, rep: Report, prev_sel: dict, check_cache: b
         kl = [pre_row for pre_row in _local_keys(run, u, A, B)] + [np64(run.kn_src[s, b, h]) for s in range(t + 1)]
         vl = list(V[w.seq_len - W:]) + [np64(run.vn_src[s, b, h]) for s in range(t + 1)]
         oo = oid[u] if oid is not None else []
-        want = ref.attend_on_index_set(q[u], A, B, V, oo, sel[u], kl, vl, C, w.rope_base, storage=w.dtype)
+        want = ref.attend_on_index_set(q[u], A, B, V, oo, sel[u], kl, vl, C, w.rope_base, storage=kd,
+                                       v_storage=ref.value_storage(w.dtype))
         exact = ref.attend_on_index_set(q[u], A, B, V, oo, sel[u], kl, vl, C, w.rope_base)
         err = np.max(np.abs(out[u] - want))
         rel = err / max(np.max(np.abs(want)), 1e-30)
         rep.max_out_err = max(rep.max_out_err, err)
         rep.max_out_rel = max(rep.max_out_rel, rel)
         rep.max_err_vs_unrounded = max(rep.max_err_vs_unrounded, float(np.max(np.abs(out[u] - exact))))
-        if w.dtype == "bf16":
+        if w.dtype in ("bf16", "fp8"):
             assert err <= 2e-2, f"output abs error {err} (unit {u}, step {t})"
         else:
             assert rel <= 1e-4, f"output rel error {rel} (unit {u}, step {t})"
