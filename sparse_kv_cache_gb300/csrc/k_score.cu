@@ -405,7 +405,7 @@ struct ScTile8 {
 };
 
 template <int G>
-__global__ void __launch_bounds__(192, 1) k_score_f8(const __grid_constant__ CUtensorMap tmL, ScoreParams p) {
+__global__ void __launch_bounds__(320, 1) k_score_f8(const __grid_constant__ CUtensorMap tmL, ScoreParams p) {
     constexpr int NQ = (3 * G <= 16) ? 16 : 32;   // MMA N: the 3G term rows, padded
     constexpr int kQBytes = NQ * 128;
     constexpr int kT8 = 2 * kScTile;              // 256 landmarks per stage: two M = 128 halves
@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(192, 1) k_score_f8(const __grid_constant__ CUt
     const int64_t n_c = p.n_c;
     if (tid == 0) {
         for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-        for (int b = 0; b < 2; ++b) { mbar_init(&accf[b], 2); mbar_init(&acce[b], 4); }
+        for (int b = 0; b < 2; ++b) { mbar_init(&accf[b], 2); mbar_init(&acce[b], kScParts8); }
         mbar_init(&drain, 1);
         s_abort = 0;
         fence_mbar_init();
@@ -555,10 +555,12 @@ __global__ void __launch_bounds__(192, 1) k_score_f8(const __grid_constant__ CUt
         __syncwarp();
         (void)mbar_wait(&drain, 0);
     } else {
-        // ------------------------------------------------ epilogue: 4 warps, one landmark row per thread
+        // ------------------------------------------------ epilogue: 8 warps, warp (h, quarter) scores
+        // row 32*quarter + lane of half h of every stage
         const int quarter = warp & 3;                     // TMEM lanes [32*quarter, +32)
-        const int row = quarter * 32 + lane;
-        const int ew = warp - 2;
+        const int ew = warp - 2;                          // 0..7
+        const int h = ew >> 2;
+        const int rr = h * kScTile + quarter * 32 + lane;
         float m[G], sx[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) { m[g] = -CUDART_INF_F; sx[g] = 0.f; }
@@ -573,27 +575,22 @@ __global__ void __launch_bounds__(192, 1) k_score_f8(const __grid_constant__ CUt
             if (t.run < 0) break;
             tc_fence_after();
             constexpr int NC8 = (3 * G + 7) / 8;
-            float v[2][NC8 * 8];
+            float v[NC8 * 8];
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
+            for (int c8 = 0; c8 < NC8; ++c8) {
+                float w[8];
+                tmem_ld8(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + (2 * b + h) * NQ + 8 * c8, w);
 #pragma unroll
-                for (int c8 = 0; c8 < NC8; ++c8) {
-                    float w[8];
-                    tmem_ld8(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + (2 * b + h) * NQ + 8 * c8, w);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) v[h][8 * c8 + kk] = w[kk];
-                }
+                for (int kk = 0; kk < 8; ++kk) v[8 * c8 + kk] = w[kk];
+            }
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acce[b]);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int rr = h * kScTile + row;
-                if (rr >= t.nv) continue;
+            if (rr < t.nv) {
                 float z[G];
 #pragma unroll
-                for (int g = 0; g < G; ++g) z[g] = (v[h][g] + v[h][G + g] + v[h][2 * G + g]) * t.inv[g] * p.scale;
+                for (int g = 0; g < G; ++g) z[g] = (v[g] + v[G + g] + v[2 * G + g]) * t.inv[g] * p.scale;
                 float* dst = p.logits + (t.j + rr) * G;
                 if constexpr (G == 4) {
                     *reinterpret_cast<float4*>(dst) = make_float4(z[0], z[1], z[2], z[3]);
@@ -617,7 +614,7 @@ __global__ void __launch_bounds__(192, 1) k_score_f8(const __grid_constant__ CUt
                     const float M = warp_max(m[g]);
                     const float tt = (m[g] == -CUDART_INF_F) ? 0.f : sx[g] * __expf(m[g] - M);
                     const float Ssum = warp_sum(tt);
-                    if (lane == 0) p.part[(static_cast<int64_t>(t.run) * kScParts + ew) * G + g] = make_float2(M, Ssum);
+                    if (lane == 0) p.part[(static_cast<int64_t>(t.run) * kScParts8 + ew) * G + g] = make_float2(M, Ssum);
                     m[g] = -CUDART_INF_F;
                     sx[g] = 0.f;
                 }
@@ -632,52 +629,59 @@ __global__ void __launch_bounds__(192, 1) k_score_f8(const __grid_constant__ CUt
     }
 }
 
-// The query terms of the e5m2 scorer, once per step: block u, thread = dimension; per head
-// the largest |q| over the 128 dimensions sets 2^s (largest power of two with
-// max|q| * 2^s < 2^14), then x = q * 2^s gives t1 = e5m2(x), t2 = e5m2(x - t1),
+// The query terms of the e5m2 scorer, once per step: block u, warp g = head, lane l = dims
+// [4l, 4l + 4).  Per head the largest |q| over the 128 dimensions sets 2^s (largest power of two
+// with max|q| * 2^s < 2^14), then x = q * 2^s gives t1 = e5m2(x), t2 = e5m2(x - t1),
 // t3 = e5m2(x - t1 - t2) into rows jt*G + g of qt[u], and qinv[u][g] = 2^-s.
 template <int G>
-__global__ void __launch_bounds__(kD) k_qsplit(const __nv_bfloat16* __restrict__ q, uint8_t* __restrict__ qt,
-                                               float* __restrict__ qinv) {
-    __shared__ float red[4];
-    const int u = blockIdx.x, dim = threadIdx.x, lane = dim & 31, warp = dim >> 5;
-#pragma unroll 1
-    for (int g = 0; g < G; ++g) {
-        const float x0 = __bfloat162float(q[(static_cast<int64_t>(u) * G + g) * kD + dim]);
-        float mx = warp_max(fabsf(x0));
-        if (lane == 0) red[warp] = mx;
-        __syncthreads();
-        mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-        __syncthreads();
-        int sh = 0;
-        if (mx > 0.f) {
-            int ex;
-            frexpf(mx, &ex);               // mx in [2^(ex-1), 2^ex)
-            sh = max(-100, min(100, 14 - ex));
-        }
-        float r = x0 * ldexpf(1.f, sh);
-        uint8_t* row = qt + static_cast<int64_t>(u) * 3 * G * kD;
+__global__ void __launch_bounds__(32 * G) k_qsplit(const __nv_bfloat16* __restrict__ q, uint8_t* __restrict__ qt,
+                                                   float* __restrict__ qinv) {
+    pdl_wait();
+    pdl_trigger();
+    const int u = blockIdx.x, g = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint2 raw = reinterpret_cast<const uint2*>(q + (static_cast<int64_t>(u) * G + g) * kD)[lane];
+    const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+    float x[4];
+    const float2 a = __bfloat1622float2(q2[0]), c = __bfloat1622float2(q2[1]);
+    x[0] = a.x; x[1] = a.y; x[2] = c.x; x[3] = c.y;
+    const float mx = warp_max(fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))));
+    int sh = 0;
+    if (mx > 0.f) {
+        int ex;
+        frexpf(mx, &ex);   // mx in [2^(ex-1), 2^ex)
+        sh = max(-100, min(100, 14 - ex));
+    }
+    const float up = ldexpf(1.f, sh);
+    uint32_t word[3] = {0u, 0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        float r = x[e] * up;
 #pragma unroll
         for (int jt = 0; jt < 3; ++jt) {
-            const uint32_t b8 = from_f<__nv_fp8_e5m2>(r).__x;
-            row[(jt * G + g) * kD + dim] = static_cast<uint8_t>(b8);
+            const uint32_t b8 = from_f<__nv_fp8_e5m2>(r).__x & 0xffu;
+            word[jt] |= b8 << (8 * e);
             r -= e5m2_to_f(b8);
         }
-        if (dim == 0) qinv[u * G + g] = ldexpf(1.f, -sh);
     }
+    uint8_t* row = qt + static_cast<int64_t>(u) * 3 * G * kD;
+#pragma unroll
+    for (int jt = 0; jt < 3; ++jt) reinterpret_cast<uint32_t*>(row + (jt * G + g) * kD)[lane] = word[jt];
+    if (lane == 0) qinv[u * G + g] = ldexpf(1.f, -sh);
 }
 
 int launch_qsplit(const void* q, void* qt, float* qinv, int U, int G, cudaStream_t s) {
     auto q16 = static_cast<const __nv_bfloat16*>(q);
     auto qt8 = static_cast<uint8_t*>(qt);
+    cudaError_t e = cudaErrorInvalidValue;
     switch (G) {
-        case 1: k_qsplit<1><<<U, kD, 0, s>>>(q16, qt8, qinv); break;
-        case 2: k_qsplit<2><<<U, kD, 0, s>>>(q16, qt8, qinv); break;
-        case 4: k_qsplit<4><<<U, kD, 0, s>>>(q16, qt8, qinv); break;
-        case 8: k_qsplit<8><<<U, kD, 0, s>>>(q16, qt8, qinv); break;
+        case 1: e = launch_pdl(k_qsplit<1>, dim3(U), dim3(32), 0, s, q16, qt8, qinv); break;
+        case 2: e = launch_pdl(k_qsplit<2>, dim3(U), dim3(64), 0, s, q16, qt8, qinv); break;
+        case 4: e = launch_pdl(k_qsplit<4>, dim3(U), dim3(128), 0, s, q16, qt8, qinv); break;
+        case 8: e = launch_pdl(k_qsplit<8>, dim3(U), dim3(256), 0, s, q16, qt8, qinv); break;
         default: return -1;
     }
-    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+    if (e != cudaSuccess) { cudaGetLastError(); return -1; }
+    return 0;
 }
 
 template <int G>
@@ -685,7 +689,7 @@ static int launch_f8(const CUtensorMap* tmL, const ScoreParams& p, int ncta, cud
     constexpr int NQ = (3 * G <= 16) ? 16 : 32;
     const int smem = kScStages8 * (32768 + NQ * 128) + 1024;
     cudaFuncSetAttribute(k_score_f8<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (launch_pdl(k_score_f8<G>, dim3(ncta), dim3(192), smem, s, *tmL, p) != cudaSuccess) {
+    if (launch_pdl(k_score_f8<G>, dim3(ncta), dim3(320), smem, s, *tmL, p) != cudaSuccess) {
         cudaGetLastError();
         return -1;
     }
@@ -748,7 +752,7 @@ int launch_score(int dtype, int G, const CUtensorMap* tmL, const ScoreParams& p,
     }
 }
 
-int score_parts(int dtype) { return dtype != 0 ? kScParts : kScoreWarps; }
+int score_parts(int dtype) { return dtype == 2 ? kScParts8 : dtype != 0 ? kScParts : kScoreWarps; }
 
 int score_ctas_per_sm(int dtype, int G) {
     if (dtype != 0) {

@@ -26,6 +26,7 @@ constexpr int kScStages = 6;
 constexpr int kScStages8 = 6;   // e5m2 scorer: 2 x 16 KB tiles + query terms per stage
 constexpr int kScN = 16;          // MMA N: the G <= 8 query heads, zero-padded
 constexpr int kScParts = 4;       // partial records per (CTA, unit): one per epilogue warp
+constexpr int kScParts8 = 8;      // the e5m2 scorer's epilogue warps: two per TMEM lane quarter
 
 constexpr int kRunChunks = 512;   // landmarks per unit of scheduled scoring work
 
