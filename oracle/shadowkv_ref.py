@@ -29,6 +29,9 @@ Readings where the pages are silent (each is also listed in the design notes):
   exact and are neither landmarks nor selectable.
 * The softmax of the selection runs over the n_c selectable chunks only.
 * The query and the new key arrive post-RoPE at position S+t.
+* ShadowKV+ (generated keys at rank r): the new key arrives pre-RoPE, over all
+  H heads of its batch element, and is kept only as k' Psi with Psi = B^T; at
+  every step each generated token's key is rebuilt as RoPE(a.B_h) at S+t.
 
 Parity pins: see ``tests/test_oracle_pins.py`` and ``tests/test_golden.py``.
 The selection scores' near-tie band is not pinned by the pages (no page prints
@@ -252,6 +255,35 @@ def attend_on_index_set(q_group, A_b, B_bh, V_bh, outlier_ids, sel_ids, k_local,
     V = np.concatenate([V_bh[to], V_bh[ts],
                         round_to_storage(np.asarray(v_local, np.float64).reshape(-1, d), v_storage)])
     return attend(q_group, K, V)
+
+
+# ----------------------------------------------------------------------------
+# ShadowKV+: generated tokens' keys kept at rank r (summary page, "The ShadowKV+
+# extension for generated tokens"; digest, section A7 "handling of newly
+# generated tokens")
+# ----------------------------------------------------------------------------
+
+
+def project_new_key(k_pre_b: np.ndarray, B_b: np.ndarray, storage: str | None = None) -> np.ndarray:
+    """Rank-r state of one generated token of one batch element: k' Psi.
+
+    k_pre_b [H][d] is the token's pre-RoPE key over the H KV heads, read as one
+    row k' of width H*d; Psi is the context's right singular basis, which is B_b
+    [H][r][d] read as the [r][H*d] matrix B = Psi^T.  The result a = k' Psi [r]
+    is held in the storage dtype, as the context rows of A are.
+    """
+    B = np.asarray(B_b, np.float64)
+    H, r, d = B.shape
+    Psi_T = B.transpose(1, 0, 2).reshape(r, H * d)          # row j: (B[0][j], ..., B[H-1][j])
+    k = np.asarray(k_pre_b, np.float64).reshape(H * d)
+    return round_to_storage(Psi_T @ k, storage)
+
+
+def new_token_key(a: np.ndarray, B_bh: np.ndarray, pos: int, base: float) -> np.ndarray:
+    """Key of a generated token when attention needs it: head h's slice of the
+    reconstruction (k' Psi) Psi^T is a.B_h, rotated at the token's position like
+    a rebuilt context key."""
+    return rebuild_keys(np.asarray(a, np.float64)[None, :], B_bh, np.array([pos]), base)[0]
 
 
 @dataclass

@@ -90,6 +90,21 @@ def _hit_miss_swapped(prev, cur):
 
 _orig_hit_miss = ref.hit_miss
 
+
+def _project_no_transpose(k_pre_b, B_b, storage=None):
+    B = np.asarray(B_b, np.float64)
+    H, r, d = B.shape
+    return ref.round_to_storage(B.reshape(r, H * d) @ np.asarray(k_pre_b, np.float64).reshape(H * d), storage)
+
+
+def _project_first_head_only(k_pre_b, B_b, storage=None):
+    B = np.asarray(B_b, np.float64)
+    return ref.round_to_storage(B[0] @ np.asarray(k_pre_b, np.float64)[0], storage)
+
+
+def _new_key_without_rope(a, B_bh, pos, base):
+    return np.asarray(a, np.float64) @ np.asarray(B_bh, np.float64)
+
 MUTANTS = [
     ("e5m2_round", _e5m2_ties_away, [pins.test_e5m2_round_hand_values]),
     ("apply_rope", _rope_wrong_sign, [pins.test_rope_closed_form_basis_vectors]),
@@ -103,6 +118,11 @@ MUTANTS = [
     ("arg_topk", _topk_upper_ties, [pins.test_arg_topk_matches_brute_force_with_ties]),
     ("prefill_unit", _prefill_no_outlier_kv, [pins.test_full_rank_full_budget_equals_dense_causal_attention]),
     ("hit_miss", _hit_miss_swapped, [pins.test_hit_miss_matches_python_sets]),
+    ("project_new_key", _project_no_transpose, [pins.test_plus_projection_closed_form_in_span,
+                                                pins.test_plus_projection_brute_force]),
+    ("project_new_key", _project_first_head_only, [pins.test_plus_projection_closed_form_in_span,
+                                                   pins.test_plus_projection_brute_force]),
+    ("new_token_key", _new_key_without_rope, [pins.test_plus_full_rank_equals_exact_new_keys]),
 ]
 
 

@@ -367,3 +367,82 @@ def test_fp8_storage_readings():
     assert ref.key_storage("bf16") == "bf16" and ref.value_storage("bf16") == "bf16"
     x = np.array([1.1, -0.3, 2.0 ** -17])
     np.testing.assert_array_equal(ref.round_to_storage(x, "e5m2"), [1.0, -0.3125, 0.0])
+
+
+# --------------------------------------------------------------------- ShadowKV+ (generated keys at rank r)
+
+
+def _orthonormal_basis(rng, n, r):
+    """[n][r] with orthonormal columns."""
+    q, _ = np.linalg.qr(rng.standard_normal((n, r)))
+    return q
+
+
+def _B_from_basis(Q, H, d):
+    """B_b [H][r][d] whose [r][H*d] reading is Q^T (Psi = Q)."""
+    return np.stack([Q[h * d:(h + 1) * d, :].T for h in range(H)])
+
+
+def test_plus_projection_closed_form_in_span():
+    rng = np.random.default_rng(31)
+    H, d, r = 3, 8, 5
+    Q = _orthonormal_basis(rng, H * d, r)
+    B = _B_from_basis(Q, H, d)
+    c = rng.standard_normal(r)
+    k = (Q @ c).reshape(H, d)                       # a key inside the context's subspace
+    a = ref.project_new_key(k, B)
+    np.testing.assert_allclose(a, c, rtol=0, atol=1e-12)
+    for h in range(H):                              # position 0: RoPE is the identity
+        np.testing.assert_allclose(ref.new_token_key(a, B[h], 0, 10000.0), k[h], rtol=0, atol=1e-12)
+
+
+def test_plus_projection_drops_the_orthogonal_part():
+    rng = np.random.default_rng(32)
+    H, d, r = 2, 8, 3
+    Q = _orthonormal_basis(rng, H * d, r)
+    B = _B_from_basis(Q, H, d)
+    c = rng.standard_normal(r)
+    g = rng.standard_normal(H * d)
+    z = g - Q @ (Q.T @ g)                           # orthogonal to the subspace
+    a = ref.project_new_key((Q @ c + z).reshape(H, d), B)
+    np.testing.assert_allclose(a, c, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(ref.project_new_key(z.reshape(H, d), B), 0.0, rtol=0, atol=1e-12)
+
+
+def test_plus_projection_brute_force():
+    rng = np.random.default_rng(33)
+    H, r, d = 3, 5, 4
+    B = rng.standard_normal((H, r, d))              # any basis: the definition is the plain sum
+    k = rng.standard_normal((H, d))
+    want = np.zeros(r)
+    for j in range(r):
+        for h in range(H):
+            for i in range(d):
+                want[j] += k[h, i] * B[h, j, i]
+    np.testing.assert_allclose(ref.project_new_key(k, B), want, rtol=0, atol=1e-12)
+    # stored in bf16 like the context rows of A
+    np.testing.assert_array_equal(ref.project_new_key(k, B, "bf16"), ref.bf16_round(want))
+
+
+def test_plus_full_rank_equals_exact_new_keys():
+    """With r = H*d and an orthogonal basis the projection loses nothing, so
+    ShadowKV+ must give the same outputs as ShadowKV fed the exact post-RoPE
+    new keys."""
+    c = _dense_case(seed=34, steps=3)
+    H, d, r, S, base = c["H"], c["d"], c["r"], c["S"], 500000.0
+    rng = np.random.default_rng(35)
+    Q = _orthonormal_basis(rng, r, r)               # square: orthogonal
+    B = _B_from_basis(Q, H, d)                      # [H][r][d]
+    A = np.concatenate([c["keys"][h] for h in range(H)], axis=1) @ Q   # A.B_h = keys_h
+    kpre = c["kn"]                                  # [T][H][d], pre-RoPE in this case
+    for h in range(H):
+        st_exact = ref.UnitDecodeState(ref.prefill_unit(A, B[h], c["V"][h], c["C"], c["O"], c["W"], base))
+        st_plus = ref.UnitDecodeState(ref.prefill_unit(A, B[h], c["V"][h], c["C"], c["O"], c["W"], base))
+        for t in range(c["steps"]):
+            qg = c["qs"][t, h * c["G"]:(h + 1) * c["G"]]
+            k_exact = _rope_complex(kpre[t, h][None, :], np.array([S + t]), base)[0]
+            k_plus = ref.new_token_key(ref.project_new_key(kpre[t], B), B[h], S + t, base)
+            r1 = ref.decode_step_unit(st_exact, qg, k_exact, c["vn"][t, h], A, B[h], c["V"][h], 6, c["C"], base)
+            r2 = ref.decode_step_unit(st_plus, qg, k_plus, c["vn"][t, h], A, B[h], c["V"][h], 6, c["C"], base)
+            assert np.array_equal(r1["sel"], r2["sel"])
+            np.testing.assert_allclose(r2["out"], r1["out"], rtol=0, atol=1e-11)

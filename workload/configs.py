@@ -37,6 +37,7 @@ class Workload:
     ar_rho: float = 0.95  # AR(1) coefficient of A rows along tokens
     spike_chunks: int = -1     # planted outlier chunks per batch element (-1: 0.3 % of chunks, capped at O)
     spike_scale: float = 6.0
+    new_keys: str = "exact"    # "exact": generated keys kept whole; "lowrank": ShadowKV+ (kept at rank r)
 
     @property
     def group(self) -> int:

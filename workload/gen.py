@@ -9,12 +9,18 @@ here.  The recipe (one seeded torch generator per layer and purpose):
   without replacement outside the local window; the A rows of their odd token
   offsets are replaced by ``spike_scale * N(0,1)``.
 * B [b][H][r][d] ~ N(0, 1/r), so every pre-RoPE key coordinate has variance 1.
+  For ShadowKV+ workloads (``new_keys == "lowrank"``) B is the right singular
+  basis an SVD would give: B_b read as [r][H*d] has orthonormal rows (QR of a
+  Gaussian matrix), and A is scaled by sqrt(H*d/r) so that the keys keep unit
+  per-coordinate variance.
 * V [b][H][S][d] ~ N(0,1).
 * queries q [T][b][H*G][d]: q_0 ~ N(0,1), q_t = drift*q_{t-1} + sqrt(1-drift^2)*eps
   (already post-RoPE, as a model hands them to the attention).
 * new tokens k_new, v_new [T][b][H][d] ~ N(0,1): the key of a generated token
   arrives post-RoPE from the model's own projection, outside this path, so it is
-  drawn with the per-coordinate variance of the rebuilt keys.
+  drawn with the per-coordinate variance of the rebuilt keys.  For ShadowKV+
+  workloads k_new is the pre-RoPE key, drawn inside the context's subspace plus
+  a small residue: k'_t = c_t.B_b + 0.1*eps with c_t ~ N(0, H*d/r).
 
 The generator on a CUDA device uses torch's Philox stream and the one on the CPU
 uses torch's CPU stream, so the same seed gives different numbers on the two;
@@ -69,6 +75,10 @@ def spike_chunks(w: Workload, layer: int) -> torch.Tensor:
     return out
 
 
+def _lowrank_scale(w: Workload) -> float:
+    return math.sqrt(w.n_kv_heads * w.head_dim / w.rank)
+
+
 def make_A(w: Workload, layer: int, device="cpu") -> torch.Tensor:
     g = _gen(w, layer, "A", device)
     e = torch.randn((w.batch, w.seq_len, w.rank), generator=g, device=device, dtype=torch.float32)
@@ -83,11 +93,21 @@ def make_A(w: Workload, layer: int, device="cpu") -> torch.Tensor:
             rows = (sp[b][:, None] * w.chunk + odd[None, :]).reshape(-1).to(device)
             A[b, rows] = w.spike_scale * torch.randn((rows.numel(), w.rank), generator=gs,
                                                      device=device, dtype=torch.float32)
+    if w.new_keys == "lowrank":
+        A *= _lowrank_scale(w)
     return A.to(storage_dtype(w))
 
 
 def make_B(w: Workload, layer: int, device="cpu") -> torch.Tensor:
     g = _gen(w, layer, "B", device)
+    if w.new_keys == "lowrank":
+        H, d, r = w.n_kv_heads, w.head_dim, w.rank
+        if r > H * d:
+            raise ValueError("a rank-r orthonormal basis needs r <= H*d")
+        G = torch.randn((w.batch, H * d, r), generator=g, device=device, dtype=torch.float64)
+        Q = torch.linalg.qr(G).Q                                  # [b][H*d][r], orthonormal columns
+        B = Q.transpose(1, 2).reshape(w.batch, r, H, d).permute(0, 2, 1, 3).contiguous()
+        return B.to(torch.float32).to(storage_dtype(w))
     B = torch.randn((w.batch, w.n_kv_heads, w.rank, w.head_dim), generator=g, device=device,
                     dtype=torch.float32) / math.sqrt(w.rank)
     return B.to(storage_dtype(w))
@@ -117,6 +137,11 @@ def make_decode_inputs(w: Workload, layer: int, steps: int | None = None, device
     gk = _gen(w, layer, "k_new", device)
     k_new = torch.randn((T, w.batch, w.n_kv_heads, w.head_dim), generator=gk, device=device,
                         dtype=torch.float32)
+    if w.new_keys == "lowrank":
+        Bf = make_B(w, layer, device).float()                     # [b][H][r][d]
+        c = torch.randn((T, w.batch, w.rank), generator=gk, device=device,
+                        dtype=torch.float32) * _lowrank_scale(w)
+        k_new = 0.1 * k_new + torch.einsum("tbj,bhjd->tbhd", c, Bf)
     gv = _gen(w, layer, "v_new", device)
     v_new = torch.randn((T, w.batch, w.n_kv_heads, w.head_dim), generator=gv, device=device,
                         dtype=torch.float32)
