@@ -36,7 +36,8 @@ SCORE_TRAFFIC = {"source_sha256": "1f96b4682ac28cf2c31680e6d4c4a093f1f6990af7e78
                  "seq_len": 131072, "dtype": "bf16", "bytes_per_unit": (133892096 + 4653568) / 32}
 
 # kernels one layer's decode step launches: score, select, gather, rebuild, attention, merge;
-# the e5m2 configuration adds the query split ahead of the scorer
+# the e5m2 configuration adds the query split ahead of the scorer; ShadowKV+ adds the projection
+# and the rebuild of the generated tokens' keys
 LAUNCHES_PER_LAYER = {"bf16": 6, "fp8": 7}
 
 METRIC = "sparse decode-attention tokens/s and HBM GB/s (% of 8 TB/s) at 128K, 1×GB300"
@@ -55,6 +56,8 @@ def parse():
     ap.add_argument("--v-place", default="", choices=["", "hbm", "host"])
     ap.add_argument("--dtype", default="", choices=["", "bf16", "fp8"],
                     help="storage: bf16, or fp8 (e5m2 landmarks and values, bf16 keys and factors)")
+    ap.add_argument("--new-keys", default="", choices=["", "exact", "lowrank"],
+                    help="lowrank: ShadowKV+ (generated tokens' keys kept at rank r and rebuilt each step)")
     ap.add_argument("--drift", type=float, default=-1.0)
     ap.add_argument("--share-storage", default="auto", choices=["auto", "yes", "no"],
                     help="reuse one layer's A/B/V for every layer (state stays per layer)")
@@ -82,6 +85,10 @@ def workload_from(args) -> Workload:
             kw["name"] = w.name + "-fp8"
     if args.drift >= 0:
         kw["drift"] = args.drift
+    if args.new_keys:
+        kw["new_keys"] = args.new_keys
+        if args.new_keys == "lowrank":
+            kw["name"] = kw.get("name", w.name) + "-plus"
     return w.with_(**kw) if kw else w
 
 
@@ -417,6 +424,7 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
                    "n_kv_heads": w.n_kv_heads, "n_q_heads": w.n_q_heads, "head_dim": w.head_dim,
                    "rank": w.rank, "chunk": w.chunk, "n_select": w.n_select, "n_outlier": w.n_outlier,
                    "local_window": w.local_window, "v_place": w.v_place, "drift": w.drift,
+                   "new_keys": w.new_keys,
                    "parallelism": f"replicas x{ws} (batch sharded, no collective)",
                    "microbatches": M,
                    "layers_share_input_storage": share,
@@ -435,7 +443,7 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
         "eq_bandwidth_check": eqbw,
         "clocks": clk,
         "e2e": e2e,
-        "gpu_launches": LAUNCHES_PER_LAYER[w.dtype] * L * M * K,
+        "gpu_launches": (LAUNCHES_PER_LAYER[w.dtype] + (2 if w.new_keys == "lowrank" else 0)) * L * M * K,
         "setup_s": setup_s,
     }
     if dev_err:

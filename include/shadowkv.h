@@ -59,6 +59,21 @@ typedef enum { SKV_F32 = 0, SKV_BF16 = 1, SKV_FP8 = 2 } skv_dtype;
 typedef enum { SKV_V_HBM = 0, SKV_V_HOST = 1 } skv_vplace;
 
 /*
+ * How the keys of generated tokens are kept.
+ * SKV_NEWKEYS_EXACT: each decode step's k_new (post-RoPE) joins the exact local
+ *   set as it is.
+ * SKV_NEWKEYS_LOWRANK: ShadowKV+ (summary page, "The ShadowKV+ extension for
+ *   generated tokens"; digest section A7 on newly generated tokens).  k_new is
+ *   the PRE-RoPE key; the library keeps only its rank-r state a = k'.Psi,
+ *   where k' [H*d] is the token's key over the H heads of its batch element and
+ *   Psi = B^T (B_b read as [r][H*d]), stored like A.  At every step each
+ *   generated token i's key is rebuilt as RoPE_{S+i}(a_i . B[b][h]), the same
+ *   reconstruction as for context keys.  For a true projection B_b's rows
+ *   should be orthonormal (B = Psi^T from the SVD); the library does not check.
+ */
+typedef enum { SKV_NEWKEYS_EXACT = 0, SKV_NEWKEYS_LOWRANK = 1 } skv_newkeys;
+
+/*
  * Sizes of one layer.  Notation of the pages: b batch, H KV heads, G = n_q/H
  * query heads per KV head, d head dim, r rank, C chunk, K selected chunks,
  * O outlier chunks, W local-window tokens, S context length.
@@ -81,6 +96,7 @@ typedef struct {
     double  rope_base;      /* theta_i = rope_base^(-2i/d), half-split pairs (i, i+d/2) */
     int32_t dtype;          /* skv_dtype: storage of A, B, V, q, keys, landmarks, out (SKV_FP8: see above) */
     int32_t v_place;        /* skv_vplace of V */
+    int32_t new_keys;       /* skv_newkeys */
 } skv_config;
 
 typedef struct skv_layer skv_layer;   /* opaque; one per layer */
@@ -127,7 +143,9 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
  *      cached tokens and the W + t + 1 local tokens (t = 0-based step).
  *
  *   q      dev [b][H*G][d]  post-RoPE queries at position S + t
- *   k_new  dev [b][H][d]    post-RoPE key of the new token
+ *   k_new  dev [b][H][d]    post-RoPE key of the new token (SKV_NEWKEYS_LOWRANK:
+ *                           its pre-RoPE key; step 1 then stores a = k'.Psi and
+ *                           step 4 also rebuilds every generated token's key)
  *   v_new  dev [b][H][d]
  *   out    dev [b][H*G][d]  written
  *   sel_out dev int32 [b][H][K] or NULL: I as original chunk ids, ascending
@@ -189,6 +207,9 @@ int shadowkv_set_profiling(skv_layer* layer, int enable);
 #define SKV_F_SLOT_OF_SEL  11   /* [b*H][K] int32: cache slot of each entry of I */
 #define SKV_F_MISS_COUNT   12   /* [b*H] int32: misses of the last step */
 #define SKV_F_HITS_PER_STEP 13  /* [max_new_tokens] int32: hits summed over units */
+#define SKV_F_A_NEW        14   /* [b][max_new_tokens][r] (A's storage: bf16, fp32 for SKV_F32):
+                                   rank-r states of generated tokens (SKV_NEWKEYS_LOWRANK;
+                                   size 0 otherwise) */
 #define SKV_NFIELD         14
 int64_t shadowkv_export_size(const skv_layer* layer, int field);
 int shadowkv_export(skv_layer* layer, int field, void* dst, size_t bytes, skv_stream stream);

@@ -19,8 +19,9 @@ PHASES = ("score", "select", "rebuild", "fetch", "attn")
 FIELDS = {
     "landmarks": 0, "chunk_ids": 1, "outlier_ids": 2, "min_cos": 3, "k_outlier": 4, "v_outlier": 5,
     "k_local": 6, "v_local": 7, "k_cache": 8, "v_cache": 9, "selection": 10, "slot_of_sel": 11,
-    "miss_count": 12, "hits_per_step": 13,
+    "miss_count": 12, "hits_per_step": 13, "a_new": 14,
 }
+NEW_KEYS = {"exact": 0, "lowrank": 1}
 ERRORS = {0: "OK", -1: "INVALID", -2: "OOM", -3: "NOT_PINNED", -4: "CUDA", -5: "DEVICE_BOUNDS",
           -6: "TIMEOUT", -7: "STEP_LIMIT", -8: "UNSUPPORTED"}
 EXPORTED = ("shadowkv_validate_config", "shadowkv_prefill_index", "shadowkv_decode_step",
@@ -37,7 +38,8 @@ class SkvConfig(ctypes.Structure):
                 ("n_select", ctypes.c_int32), ("n_outlier", ctypes.c_int32),
                 ("local_window", ctypes.c_int32), ("max_new_tokens", ctypes.c_int32),
                 ("seq_len", ctypes.c_int64), ("rope_base", ctypes.c_double),
-                ("dtype", ctypes.c_int32), ("v_place", ctypes.c_int32)]
+                ("dtype", ctypes.c_int32), ("v_place", ctypes.c_int32),
+                ("new_keys", ctypes.c_int32)]
 
 
 class SkvStats(ctypes.Structure):
@@ -132,7 +134,8 @@ def make_config(w=None, **kw) -> SkvConfig:
                  n_outlier=w.n_outlier, local_window=w.local_window, max_new_tokens=w.steps,
                  seq_len=w.seq_len, rope_base=w.rope_base,
                  dtype=DTYPE_CODES[w.dtype],
-                 v_place=SKV_V_HOST if w.v_place == "host" else SKV_V_HBM)
+                 v_place=SKV_V_HOST if w.v_place == "host" else SKV_V_HBM,
+                 new_keys=NEW_KEYS[w.new_keys])
     f.update(kw)
     return SkvConfig(**f)
 

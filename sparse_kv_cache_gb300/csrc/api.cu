@@ -78,6 +78,10 @@ struct skv_layer {
     CUtensorMap tmKall{};                 // the key blocks, [U*R][128], 128-row boxes (attention)
     int score_ncta = 0, score_nru = 0, score_nparts = 0, sel_smem_cap = 0;
     int32_t* sched = nullptr;
+    int newkeys = SKV_NEWKEYS_EXACT;
+    int Tpad = 0;                         // max_new_tokens rounded up to whole chunks
+    void* Anew = nullptr;                 // ShadowKV+: rank-r states of generated tokens, [b][Tpad][r]
+    CUtensorMap tmAnew{};
     uint8_t* qt = nullptr;                // e5m2 scorer: the query's three terms, [U][3G][d]
     float* qinv = nullptr;                // e5m2 scorer: 2^-s per head, [U][G]
     int64_t t = 0, t_reset = 0;
@@ -200,6 +204,13 @@ void step_bytes(const skv_config& c, int64_t t, double misses, double* hbm, doub
     double h = U * d * (es * 2.0 * G + esl * n_c + (es + esv) * (O * C + K * C + loc + 1.0));
     h += misses * C * (es * r + es * d + esv * d);   // A rows read, K and V rows written into slots
     h += (misses > 0 ? U : 0.0) * es * r * d;        // B slices
+    if (c.new_keys == SKV_NEWKEYS_LOWRANK) {
+        // ShadowKV+: the append writes no key (-U d), the projection reads k' (+U d) and B (U r d)
+        // and writes a (b r); the rebuild of the generated tokens, whole chunks at a time, reads
+        // their rank-r rows (b rows r) and B again (U r d) and writes their keys (U rows d)
+        const double rows = std::ceil((t + 1) / C) * C;
+        h += es * (2.0 * U * r * d + c.batch * r * (1.0 + rows) + U * rows * d);
+    }
     double l = misses * C * d * esv;                 // value rows over the host link
     if (c.v_place == SKV_V_HBM) { h += l; l = 0.0; }
     const double nsplit = std::ceil((O * C + K * C + loc) / attn_segment(c.dtype));
@@ -248,6 +259,9 @@ int shadowkv_validate_config(const skv_config* c) {
     if (!(c->rope_base > 1.0) || !std::isfinite(c->rope_base)) return SKV_ERR_INVALID;
     if (c->dtype != SKV_F32 && c->dtype != SKV_BF16 && c->dtype != SKV_FP8) return SKV_ERR_INVALID;
     if (c->v_place != SKV_V_HBM && c->v_place != SKV_V_HOST) return SKV_ERR_INVALID;
+    if (c->new_keys != SKV_NEWKEYS_EXACT && c->new_keys != SKV_NEWKEYS_LOWRANK) return SKV_ERR_INVALID;
+    if (c->new_keys == SKV_NEWKEYS_LOWRANK && c->seq_len + c->max_new_tokens + kC > (int64_t(1) << 31) - 1)
+        return SKV_ERR_INVALID;
     return SKV_OK;
 }
 
@@ -317,8 +331,11 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
     h->es_v = es_v_of(c.dtype);
     h->tc = c.dtype != SKV_F32;
     h->nkb = (h->r + 63) / 64;
-    h->loc_cap = h->W + h->Tmax;
-    h->nhi = static_cast<int>((c.seq_len + 255) / 256);
+    h->newkeys = c.new_keys;
+    h->Tpad = (h->Tmax + kC - 1) / kC * kC;
+    // ShadowKV+ rebuilds generated keys a whole chunk (8 rows) at a time
+    h->loc_cap = h->W + (h->newkeys == SKV_NEWKEYS_LOWRANK ? h->Tpad : h->Tmax);
+    h->nhi = static_cast<int>((c.seq_len + (h->newkeys == SKV_NEWKEYS_LOWRANK ? h->Tpad : 0) + 255) / 256);
     h->A = A;
     h->B = B;
     h->V = V;
@@ -383,6 +400,8 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
         (rc = alloc_t(h, &h->score_part, static_cast<size_t>(U) * h->score_nru * h->score_nparts * G)) ||
         (rc = alloc_t(h, &h->sched, 1)) ||
         (rc = alloc_t(h, &h->qt, static_cast<size_t>(U) * 3 * G * kD)) ||
+        (h->newkeys == SKV_NEWKEYS_LOWRANK &&
+         (rc = alloc(h, &h->Anew, static_cast<size_t>(c.batch) * h->Tpad * h->r * h->es))) ||
         (rc = alloc_t(h, &h->qinv, static_cast<size_t>(U) * G)) ||
         (rc = alloc_t(h, &h->vbuf, std::max(U * nc, static_cast<size_t>(U) * h->ncand))) ||
         (rc = alloc_t(h, &h->attn_cnt, static_cast<size_t>(U))) ||
@@ -435,13 +454,15 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
     cudaMemsetAsync(h->hits_step, 0, h->Tmax * sizeof(int32_t), s);
     cudaMemsetAsync(h->miss_count, 0, U * sizeof(int32_t), s);
     cudaMemsetAsync(h->sched, 0, sizeof(int32_t), s);
+    if (h->Anew) cudaMemsetAsync(h->Anew, 0, static_cast<size_t>(c.batch) * h->Tpad * h->r * h->es, s);
     if (h->tc) {
         if (launch_transpose_B(B, h->Bt, U, h->r, s)) return fail(SKV_ERR_CUDA);
         if ((rc = make_map(&h->tmA, A, h->r, static_cast<uint64_t>(c.batch) * c.seq_len, 8)) ||
             (rc = make_map(&h->tmB, h->Bt, h->r, static_cast<uint64_t>(U) * kD, 128)) ||
             (rc = h->dtype == SKV_FP8 ? make_map_u8(&h->tmL, h->L, kD, static_cast<uint64_t>(U) * h->n_c, kScTile)
                                       : make_map(&h->tmL, h->L, kD, static_cast<uint64_t>(U) * h->n_c, kScTile)) ||
-            (rc = make_map(&h->tmKall, h->Kall, kD, static_cast<uint64_t>(U) * h->R, 128)))
+            (rc = make_map(&h->tmKall, h->Kall, kD, static_cast<uint64_t>(U) * h->R, 128)) ||
+            (h->Anew && (rc = make_map(&h->tmAnew, h->Anew, h->r, static_cast<uint64_t>(c.batch) * h->Tpad, 8))))
             return fail(rc);
     }
 
@@ -555,7 +576,7 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     sel.prev_ids = h->sel_ids[t & 1]; sel.prev_slot = h->sel_slot[t & 1];
     sel.cur_ids = h->sel_ids[(t + 1) & 1]; sel.cur_slot = h->sel_slot[(t + 1) & 1];
     sel.miss_chunk = h->miss_chunk; sel.miss_slot = h->miss_slot; sel.miss_count = h->miss_count;
-    sel.hits_step = h->hits_step; sel.k_new = k_new; sel.v_new = v_new; sel.k_loc = h->Kloc; sel.v_loc = h->Vloc;
+    sel.hits_step = h->hits_step; sel.k_new = h->newkeys == SKV_NEWKEYS_LOWRANK ? nullptr : k_new; sel.v_new = v_new; sel.k_loc = h->Kloc; sel.v_loc = h->Vloc;
     sel.loc_cap = h->loc_cap; sel.loc_pitch = h->R; sel.W = h->W; sel.es = h->es; sel.es_v = h->es_v;
     sel.err = h->err;
     if (launch_select_decode(h->dtype, sel, sm)) return SKV_ERR_CUDA;
@@ -583,6 +604,23 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     const int gx = (K + kTileChunks - 1) / kTileChunks;
     const int rc = h->tc ? launch_rebuild_tc(&h->tmA, &h->tmB, rp, gx, sm) : launch_rebuild_f32(rp, gx, sm);
     if (rc) return SKV_ERR_CUDA;
+    if (h->newkeys == SKV_NEWKEYS_LOWRANK) {
+        // ShadowKV+: keep the new token as a = k'.Psi, then rebuild every generated token's key
+        // RoPE_{S+i}(a_i . B_h) into local rows W + i, whole chunks at a time
+        const int batch = U / h->H;
+        if (launch_project(h->dtype == SKV_F32 ? 0 : 1, k_new, h->B, h->Anew, batch, h->H, h->r, h->Tpad, t, sm))
+            return SKV_ERR_CUDA;
+        const int nch = t / kC + 1;
+        RebuildParams rn = rp;
+        rn.S = h->Tpad; rn.pos_base = h->S; rn.nchunk = h->Tpad / kC;
+        rn.list = nullptr; rn.list_us = 0; rn.list_base = 0; rn.list_cap = h->Tpad / kC;
+        rn.cnt = nullptr; rn.count_const = nch; rn.dst_idx = nullptr; rn.dst_cap = h->Tpad / kC;
+        rn.dst = static_cast<uint8_t*>(h->Kloc) + static_cast<size_t>(h->W) * kD * h->es;
+        rn.A = h->Anew;
+        const int gxn = (nch + kTileChunks - 1) / kTileChunks;
+        if (h->tc ? launch_rebuild_tc(&h->tmAnew, &h->tmB, rn, gxn, sm) : launch_rebuild_f32(rn, gxn, sm))
+            return SKV_ERR_CUDA;
+    }
     if (h->profiling) cudaEventRecord(ev[3], sm);
     if (ss != sm) cudaStreamWaitEvent(sm, h->ev_fetch, 0);
     // a7: attention over outliers + cache + local, split-K with an in-kernel merge
@@ -685,14 +723,16 @@ int64_t shadowkv_export_size(const skv_layer* h, int field) {
         case SKV_F_MIN_COS: return U * h->ncand * 4;
         case SKV_F_K_OUTLIER: return U * h->O * kC * row;
         case SKV_F_V_OUTLIER: return U * h->O * kC * row_v;
-        case SKV_F_K_LOCAL: return U * h->loc_cap * row;
-        case SKV_F_V_LOCAL: return U * h->loc_cap * row_v;
+        case SKV_F_K_LOCAL: return U * (h->W + h->Tmax) * row;
+        case SKV_F_V_LOCAL: return U * (h->W + h->Tmax) * row_v;
         case SKV_F_K_CACHE: return U * h->K * kC * row;
         case SKV_F_V_CACHE: return U * h->K * kC * row_v;
         case SKV_F_SELECTION:
         case SKV_F_SLOT_OF_SEL: return U * h->K * 4;
         case SKV_F_MISS_COUNT: return U * 4;
         case SKV_F_HITS_PER_STEP: return static_cast<int64_t>(h->Tmax) * 4;
+        case SKV_F_A_NEW:
+            return h->Anew ? static_cast<int64_t>(U / h->H) * h->Tmax * h->r * h->es : 0;
         default: return -1;
     }
 }
@@ -717,14 +757,24 @@ int shadowkv_export(skv_layer* h, int field, void* dst, size_t bytes, skv_stream
         case SKV_F_SLOT_OF_SEL: src = h->sel_slot[cur]; break;
         case SKV_F_MISS_COUNT: src = h->miss_count; break;
         case SKV_F_HITS_PER_STEP: src = h->hits_step; break;
+        case SKV_F_A_NEW: src = h->Anew; break;
     }
     if (need == 0) return SKV_OK;
     // fields inside the per-unit key/value blocks: [U][rows][d] out of rows of pitch R
     int64_t rows = 0;
     switch (field) {
         case SKV_F_K_OUTLIER: case SKV_F_V_OUTLIER: rows = static_cast<int64_t>(h->O) * kC; break;
-        case SKV_F_K_LOCAL: case SKV_F_V_LOCAL: rows = h->loc_cap; break;
+        case SKV_F_K_LOCAL: case SKV_F_V_LOCAL: rows = h->W + h->Tmax; break;
         case SKV_F_K_CACHE: case SKV_F_V_CACHE: rows = static_cast<int64_t>(h->K) * kC; break;
+    }
+    if (field == SKV_F_A_NEW) {   // [b][Tmax][r] out of [b][Tpad][r]
+        const size_t rb = static_cast<size_t>(h->Tmax) * h->r * h->es;
+        if (cudaMemcpy2DAsync(dst, rb, src, static_cast<size_t>(h->Tpad) * h->r * h->es, rb, h->U / h->H,
+                              cudaMemcpyDefault, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return SKV_ERR_CUDA;
+        }
+        return SKV_OK;
     }
     if (rows > 0) {
         const bool vfield = field == SKV_F_V_OUTLIER || field == SKV_F_V_LOCAL || field == SKV_F_V_CACHE;

@@ -66,7 +66,7 @@ struct RopeRegs {
 __device__ __forceinline__ void rope_fetch(const RebuildParams& p, const TileInfo& t, RopeRegs& r) {
     const int lane = threadIdx.x & 31;
     if (t.chunk < 0) return;
-    const int pos0 = t.chunk * kC;
+    const int64_t pos0 = p.pos_base + static_cast<int64_t>(t.chunk) * kC;
     r.hi = reinterpret_cast<const float4*>(p.rope_hi + (pos0 >> 8) * (kD / 2))[lane];
 #pragma unroll
     for (int i = 0; i < kC; ++i) r.lo[i] = reinterpret_cast<const float4*>(p.rope_lo + ((pos0 + i) & 255) * (kD / 2))[lane];
@@ -344,6 +344,55 @@ __global__ void __launch_bounds__(128) k_rebuild_f32(RebuildParams p) {
         __syncthreads();
         tile_stats(p, u, ti, stage, smean);
     }
+}
+
+// ------------------------------------------------------------------ ShadowKV+ projection
+// The rank-r state of a generated token (summary page, "The ShadowKV+ extension
+// for generated tokens"): a[j] = sum over heads h and dims i of k'[h][i] * B[h][j][i],
+// i.e. k' (the token's pre-RoPE key over the H heads) times Psi = B^T.  Block
+// (b, j-group of 8), warp w -> j = 8*j-group + w; lane l covers dims [4l, 4l + 4)
+// of every head, so each head's B row is read as one contiguous 256/512-byte line.
+template <typename T>
+__global__ void __launch_bounds__(256) k_project(const T* __restrict__ k_new, const T* __restrict__ B,
+                                                 T* __restrict__ a_new, int H, int r, int64_t a_rows, int t) {
+    const int b = blockIdx.x, lane = threadIdx.x & 31, j = blockIdx.y * 8 + (threadIdx.x >> 5);
+    if (j >= r) return;
+    float acc = 0.f;
+    for (int h = 0; h < H; ++h) {
+        const T* kr = k_new + (static_cast<int64_t>(b) * H + h) * kD + 4 * lane;
+        const T* br = B + ((static_cast<int64_t>(b) * H + h) * r + j) * kD + 4 * lane;
+        float kv[4], bv[4];
+        if constexpr (sizeof(T) == 2) {
+            const uint2 kw = *reinterpret_cast<const uint2*>(kr), bw = *reinterpret_cast<const uint2*>(br);
+            const float2 k0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kw.x));
+            const float2 k1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kw.y));
+            const float2 b0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw.x));
+            const float2 b1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw.y));
+            kv[0] = k0.x; kv[1] = k0.y; kv[2] = k1.x; kv[3] = k1.y;
+            bv[0] = b0.x; bv[1] = b0.y; bv[2] = b1.x; bv[3] = b1.y;
+        } else {
+            const float4 kw = *reinterpret_cast<const float4*>(kr), bw = *reinterpret_cast<const float4*>(br);
+            kv[0] = kw.x; kv[1] = kw.y; kv[2] = kw.z; kv[3] = kw.w;
+            bv[0] = bw.x; bv[1] = bw.y; bv[2] = bw.z; bv[3] = bw.w;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc = fmaf(kv[e], bv[e], acc);
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) a_new[(static_cast<int64_t>(b) * a_rows + t) * r + j] = from_f<T>(acc);
+}
+
+int launch_project(int dtype, const void* k_new, const void* B, void* a_new, int batch, int H, int r,
+                   int64_t a_rows, int t, cudaStream_t s) {
+    const dim3 grid(batch, (r + 7) / 8);
+    if (dtype == 0)
+        k_project<float><<<grid, 256, 0, s>>>(static_cast<const float*>(k_new), static_cast<const float*>(B),
+                                              static_cast<float*>(a_new), H, r, a_rows, t);
+    else
+        k_project<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(k_new),
+                                                      static_cast<const __nv_bfloat16*>(B),
+                                                      static_cast<__nv_bfloat16*>(a_new), H, r, a_rows, t);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
 // ------------------------------------------------------------------ B transpose (bf16)

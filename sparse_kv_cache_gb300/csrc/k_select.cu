@@ -274,7 +274,10 @@ __global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
             const int64_t off = (static_cast<int64_t>(u) * p.loc_pitch + row) * kD * p.es;
             const int64_t src = static_cast<int64_t>(u) * kD * p.es;
             if (wt < n16) {
-                copy_row16(static_cast<uint8_t*>(p.k_loc) + off, static_cast<const uint8_t*>(p.k_new) + src, n16, wt, 1 << 30);
+                // no key here for generated keys kept at rank r: the rebuild writes it
+                if (p.k_new)
+                    copy_row16(static_cast<uint8_t*>(p.k_loc) + off, static_cast<const uint8_t*>(p.k_new) + src, n16,
+                               wt, 1 << 30);
             } else if (p.es_v == 1) {
                 // e5m2 value storage: 16 threads round 8 bf16 values each
                 const int vt = wt - 64;

@@ -87,7 +87,8 @@ int launch_select_outliers(const SelectParams& p, cudaStream_t s);
 struct RebuildParams {
     int mode;                 // 0: store RoPE'd keys, 1: landmark + min-cos statistics
     int U, H, r, nkb;
-    int64_t S;
+    int64_t S;                // rows of A per batch element (chunk c of batch b: rows b*S + 8c ...)
+    int64_t pos_base;         // RoPE position of chunk c's first row: pos_base + 8c
     int nchunk;               // S / C, bound on chunk ids
     const int32_t* list;      // [U][list_us] chunk ids, or NULL: chunk = list_base + index
     int64_t list_us; int list_base; int list_cap;
@@ -108,6 +109,9 @@ int launch_rebuild_tc(const CUtensorMap* tmA, const CUtensorMap* tmB, const Rebu
                       cudaStream_t s);
 int launch_rebuild_f32(const RebuildParams& p, int grid_x, cudaStream_t s);
 int launch_transpose_B(const void* B, void* Bt, int U, int r, cudaStream_t s);
+// ShadowKV+: a[b] = k'[b] . B_b^T (k' [b][H][d], B [b][H][r][d]) into row t of a_new [b][a_rows][r]
+int launch_project(int dtype, const void* k_new, const void* B, void* a_new, int batch, int H, int r,
+                   int64_t a_rows, int t, cudaStream_t s);
 
 struct GatherParams {
     const void* src; int64_t src_us;   // rows of unit u start at src + u*src_us (elements)

@@ -79,6 +79,7 @@ class LayerRun:
         self.sel = torch.empty((w.batch, w.n_kv_heads, w.n_select), dtype=torch.int32, device=dev)
         self.t = 0
         self._pre = {}
+        self._anew = {}
 
     # ------------------------------------------------------------ exports
     def export(self, field: str, dtype, shape):
@@ -101,6 +102,14 @@ class LayerRun:
     def unit_inputs(self, u: int):
         b, h = divmod(u, self.w.n_kv_heads)
         return (np64(self.A_src[b]), np64(self.B_src[b, h]), np64(self.V_src[b, h]))
+
+    def oracle_new_state(self, s: int, b: int) -> np.ndarray:
+        """ShadowKV+: a = k'.Psi of generated token s of batch element b, in A's storage."""
+        key = (s, b)
+        if key not in self._anew:
+            self._anew[key] = ref.project_new_key(np64(self.kn_src[s, b]), np64(self.B_src[b]),
+                                                  ref.key_storage(self.w.dtype))
+        return self._anew[key]
 
     def oracle_prefill(self, u: int) -> ref.UnitPrefill:
         if u not in self._pre:
@@ -255,7 +264,7 @@ def check_step(run: LayerRun, units, rep: Report, prev_sel: dict, check_cache: b
                 assert np.array_equal(vc[u][s * C:(s + 1) * C], V[tok]), "v_cache"
         # output = exact attention over the GPU's index set
         b, h = divmod(u, w.n_kv_heads)
-        kl = [pre_row for pre_row in _local_keys(run, u, A, B)] + [np64(run.kn_src[s, b, h]) for s in range(t + 1)]
+        kl = [pre_row for pre_row in _local_keys(run, u, A, B)] + [_new_key(run, s, b, h) for s in range(t + 1)]
         vl = list(V[w.seq_len - W:]) + [np64(run.vn_src[s, b, h]) for s in range(t + 1)]
         oo = oid[u] if oid is not None else []
         want = ref.attend_on_index_set(q[u], A, B, V, oo, sel[u], kl, vl, C, w.rope_base, storage=kd,
@@ -271,6 +280,32 @@ def check_step(run: LayerRun, units, rep: Report, prev_sel: dict, check_cache: b
         else:
             assert rel <= 1e-4, f"output rel error {rel} (unit {u}, step {t})"
     rep.steps += 1
+
+
+def _new_key(run: LayerRun, s: int, b: int, h: int) -> np.ndarray:
+    """Key of generated token s as attention sees it: as handed in, or (ShadowKV+)
+    rebuilt from its rank-r state k'.Psi held in A's storage dtype."""
+    w = run.w
+    if w.new_keys != "lowrank":
+        return np64(run.kn_src[s, b, h])
+    a = run.oracle_new_state(s, b)
+    return ref.new_token_key(a, np64(run.B_src[b, h]), w.seq_len + s, w.rope_base)
+
+
+def check_new_states(run: LayerRun, rep_err: list):
+    """ShadowKV+: the GPU's rank-r states of the generated tokens so far against
+    the oracle's projection, within one storage ulp (fp32 sums against float64)."""
+    w = run.w
+    t = run.t
+    a_t = run.export("a_new", run.sdtype(), (w.batch, run.steps, w.rank))
+    for b in range(w.batch):
+        for s in range(t):
+            want = run.oracle_new_state(s, b)
+            got = np64(a_t[b, s])
+            tol = (bf16_ulp(want) if w.dtype != "f32" else np.abs(want) * 2.0 ** -22) + 1e-6
+            err = np.abs(got - want)
+            assert np.all(err <= tol), f"a_new (batch {b}, step {s}): max err {err.max()}"
+            rep_err.append(float(err.max()))
 
 
 def _local_keys(run: LayerRun, u: int, A, B):
@@ -289,9 +324,12 @@ def run_and_check(w: Workload, steps: int, units=None, gen_device="cpu", check_c
     check_prefill(run, units)
     rep = Report()
     prev = {}
+    a_err = []
     for _ in range(steps):
         run.step()
         check_step(run, units, rep, prev, check_cache=check_cache)
+        if w.new_keys == "lowrank":
+            check_new_states(run, a_err)
     st = run.layer.stats()
     assert st["status"] == 0 and st["device_error"] == 0
     assert st["steps"] == steps

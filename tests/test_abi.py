@@ -86,11 +86,17 @@ def test_workload_configs_validate(lib, name):
 @pytest.mark.parametrize("field,value", [
     ("head_dim", 64), ("chunk", 16), ("rank", 12), ("rank", 264), ("n_q_heads", 12), ("n_q_heads", 48),
     ("seq_len", 4100), ("local_window", 12), ("n_select", 0), ("n_select", 5000), ("n_outlier", -1),
-    ("max_new_tokens", 0), ("dtype", 3), ("v_place", 2), ("rope_base", 0.5)])
+    ("max_new_tokens", 0), ("dtype", 3), ("v_place", 2), ("rope_base", 0.5), ("new_keys", 2),
+    ("new_keys", -1)])
 def test_invalid_configs_rejected(lib, field, value):
     cfg = lib.make_config(TINY)
     setattr(cfg, field, value)
     assert lib.validate_config(cfg) == -1
+
+
+def test_lowrank_new_keys_config_accepted(lib):
+    cfg = lib.make_config(TINY.with_(new_keys="lowrank"))
+    assert cfg.new_keys == 1 and lib.validate_config(cfg) == 0
 
 
 def test_budget_larger_than_selectable_rejected(lib):
