@@ -209,9 +209,44 @@ __device__ void topk_threshold(const float* vals, int n, int k, SelShared& sh, i
 }
 
 // Writes the selected indices (ascending) via out_fn(pos, j); returns the count.
+// Element j lives in row r = j / kSelThreads at thread j % kSelThreads, so a row
+// is in index order across the block.  One read per element: warp w counts its
+// takes in row r (a ballot), the (row, warp) counts are scanned in index order,
+// and every taken element goes to its rank.  Up to 64 rows the counts fit in
+// the histogram's storage; beyond, warps own contiguous segments (two passes).
 template <class F>
 __device__ int compact_selected(const float* vals, int n, float T, int jlast, SelShared& sh, F out_fn) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int rows = (n + kSelThreads - 1) / kSelThreads;
+    if (rows <= kBins / kWarps) {
+        int* cnt = sh.hist;   // [rows][kWarps] counts, then their exclusive prefix
+        const unsigned lt = (1u << lane) - 1u;
+        for (int r = 0; r < rows; ++r) {
+            const int j = r * kSelThreads + tid;
+            bool take = false;
+            if (j < n) { const float x = vals[j]; take = (x > T) || (x == T && j <= jlast); }
+            const unsigned bal = __ballot_sync(0xffffffffu, take);
+            if (lane == 0) cnt[r * kWarps + warp] = __popc(bal);
+        }
+        __syncthreads();
+        const int ne = rows * kWarps;
+        const int e0 = 2 * tid, e1 = e0 + 1;
+        const int c0 = e0 < ne ? cnt[e0] : 0, c1 = e1 < ne ? cnt[e1] : 0;
+        int total = 0;
+        const int base = block_exscan(c0 + c1, sh, &total);
+        if (e0 < ne) cnt[e0] = base;
+        if (e1 < ne) cnt[e1] = base + c0;
+        __syncthreads();
+        for (int r = 0; r < rows; ++r) {
+            const int j = r * kSelThreads + tid;
+            bool take = false;
+            if (j < n) { const float x = vals[j]; take = (x > T) || (x == T && j <= jlast); }
+            const unsigned bal = __ballot_sync(0xffffffffu, take);
+            if (take) out_fn(cnt[r * kWarps + warp] + __popc(bal & lt), j);
+        }
+        __syncthreads();
+        return total;
+    }
     const int seg = ((n + kWarps - 1) / kWarps + 31) & ~31;
     const int a = warp * seg, e = min(n, a + seg);
     int c = 0;
@@ -391,38 +426,36 @@ __global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
     // positions -> original chunk ids, every load in flight at once
     for (int i = tid; i < K; i += kSelThreads) sSel[i] = ids[sSel[i]];
     __syncthreads();
-    // 4. index scan against the previous step's selection
+    // 4. index scan against the previous step's selection.  Entry i's thread looks
+    // up sSel[i] among the previous ids (hit: keeps its slot) and the previous
+    // entry i among the current ids (gone: its slot is freed), two independent
+    // binary searches; misses are then numbered in order of i and freed slots in
+    // order of their previous position, and the m-th miss takes the m-th freed slot.
     const int t = p.t;
     const int32_t* pids = sPid;
     const int32_t* pslot = sPslot;
-    for (int i = tid; i < K; i += kSelThreads) {
-        int slot = -1;
-        if (t > 0) {
-            const int pidx = lower_bound(pids, K, sSel[i]);
-            if (pidx < K && pids[pidx] == sSel[i]) {
-                slot = pslot[pidx];
-                if (slot < 0 || slot >= K) { set_err(p.err, DEV_ERR_BOUNDS, 313); slot = -1; }
-            }
-        }
-        sSlot[i] = slot;
-    }
-    __syncthreads();
-    // ordered compaction of misses (by i) and of freed slots (by previous position)
-    constexpr int PER = 4;   // K <= 4096
+    constexpr int PER = (4096 + kSelThreads - 1) / kSelThreads;   // K <= 4096
+    const int per = (K + kSelThreads - 1) / kSelThreads;          // entries per thread (1 for K <= 1024)
     int mflag[PER], fflag[PER], mc = 0, fc = 0;
 #pragma unroll
     for (int r = 0; r < PER; ++r) {
-        const int i = tid * PER + r;
-        mflag[r] = (i < K) && sSlot[i] < 0;
-        int fr = 0;
-        if (i < K) {
-            if (t == 0) fr = 1;
-            else {
-                const int x = pids[i];
-                const int q = lower_bound(sSel, K, x);
-                fr = !(q < K && sSel[q] == x);
+        const int i = tid * per + r;
+        mflag[r] = fflag[r] = 0;
+        if (r >= per || i >= K) continue;
+        const int x = sSel[i];
+        int slot = -1, fr = 1;
+        if (t > 0) {
+            const int y = pids[i];
+            const int pidx = lower_bound(pids, K, x);
+            const int q = lower_bound(sSel, K, y);
+            if (pidx < K && pids[pidx] == x) {
+                slot = pslot[pidx];
+                if (slot < 0 || slot >= K) { set_err(p.err, DEV_ERR_BOUNDS, 313); slot = -1; }
             }
+            fr = !(q < K && sSel[q] == y);
         }
+        sSlot[i] = slot;
+        mflag[r] = slot < 0;
         fflag[r] = fr;
         mc += mflag[r];
         fc += fr;
@@ -433,7 +466,7 @@ __global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
     const int nmiss = both & 0xFFFF, nfree = both >> 16;
 #pragma unroll
     for (int r = 0; r < PER; ++r) {
-        const int i = tid * PER + r;
+        const int i = tid * per + r;
         if (fflag[r]) sFree[fbase++] = (t == 0) ? i : pslot[i];
     }
     __syncthreads();
@@ -444,8 +477,8 @@ __global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
     int32_t* msl = p.miss_slot + static_cast<int64_t>(u) * K;
 #pragma unroll
     for (int r = 0; r < PER; ++r) {
-        const int i = tid * PER + r;
-        if (i >= K) continue;
+        const int i = tid * per + r;
+        if (r >= per || i >= K) continue;
         int slot = sSlot[i];
         if (mflag[r]) {
             const int m = mbase++;
