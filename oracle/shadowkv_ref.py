@@ -130,18 +130,24 @@ class UnitPrefill:
     v_local: list = field(default_factory=list)
 
 
-def prefill_unit(A_b, B_bh, V_bh, C: int, O: int, W: int, base: float) -> UnitPrefill:
+def prefill_unit(A_b, B_bh, V_bh, C: int, O: int, W: int, base: float, K_exact=None) -> UnitPrefill:
     """Algorithm 1 for one (batch, KV head), with the factors A, B given.
 
-    The SVD step is out of scope: A [S][r] and B_h [r][d] are inputs, the
-    pre-RoPE keys are A.B_h and K_RoPE is their rotation at positions 0..S-1.
+    The SVD step is out of scope: A [S][r] and B_h [r][d] are inputs.  K_RoPE
+    is the rotation at positions 0..S-1 of the pre-RoPE keys: the exact keys
+    K_exact [S][d] when the caller has them (Algorithm 1 takes K and K_RoPE as
+    inputs and builds landmarks, outliers and the outlier keys from K_RoPE),
+    else A.B_h.
     """
     A_b = np.asarray(A_b, np.float64)
     V_bh = np.asarray(V_bh, np.float64)
     S = A_b.shape[0]
     n_chunk = S // C
     n_cand = n_chunk - W // C
-    K_rope = rebuild_keys(A_b, B_bh, np.arange(S), base)          # K_RoPE
+    if K_exact is not None:
+        K_rope = apply_rope(np.asarray(K_exact, np.float64), np.arange(S), base)   # K_RoPE
+    else:
+        K_rope = rebuild_keys(A_b, B_bh, np.arange(S), base)      # K_RoPE of the factors
     Cm = reduce_chunks(K_rope[: n_cand * C], C)                    # C = Reduce(K_RoPE)
     mcos = chunk_min_cos(K_rope, Cm, C)                            # Min(CosineSimilarity)
     out_ids = np.sort(arg_topk(-mcos, O))                          # ArgTopK(-Min(S), o)
@@ -236,20 +242,22 @@ def value_storage(dtype: str | None) -> str | None:
 
 def attend_on_index_set(q_group, A_b, B_bh, V_bh, outlier_ids, sel_ids, k_local, v_local,
                         C: int, base: float, storage: str | None = None,
-                        v_storage: str | None = None) -> np.ndarray:
+                        v_storage: str | None = None, k_outlier=None) -> np.ndarray:
     """Attention over [K_outlier; RoPE(K_sparse); K_local] for given index sets
     (summary page, "Assembly of the final sparse KV cache").  Keys of outlier
     and selected chunks are rebuilt here in float64 from A and B; with
     ``storage`` set, the keys the method keeps (outlier keys, rebuilt keys,
     local-window keys) take the value they have once stored in that dtype, and
     with ``v_storage`` set the local-window values likewise (context values
-    arrive already stored)."""
+    arrive already stored).  ``k_outlier`` [O*C][d] gives the outlier keys when
+    pre-filling took them from exact keys instead of the factors."""
     A_b = np.asarray(A_b, np.float64)
     V_bh = np.asarray(V_bh, np.float64)
     to = chunk_tokens(outlier_ids, C)
     ts = chunk_tokens(sel_ids, C)
     d = np.asarray(B_bh).shape[1]
-    K = np.concatenate([round_to_storage(rebuild_keys(A_b[to], B_bh, to, base), storage),
+    Ko = rebuild_keys(A_b[to], B_bh, to, base) if k_outlier is None else np.asarray(k_outlier, np.float64)
+    K = np.concatenate([round_to_storage(Ko.reshape(-1, d), storage),
                         round_to_storage(rebuild_keys(A_b[ts], B_bh, ts, base), storage),
                         round_to_storage(np.asarray(k_local, np.float64).reshape(-1, d), storage)])
     V = np.concatenate([V_bh[to], V_bh[ts],

@@ -91,6 +91,13 @@ def _hit_miss_swapped(prev, cur):
 _orig_hit_miss = ref.hit_miss
 
 
+def _prefill_ignores_exact_keys(A_b, B_bh, V_bh, C, O, W, base, K_exact=None):
+    return _orig_prefill_unit(A_b, B_bh, V_bh, C, O, W, base)
+
+
+_orig_prefill_unit = ref.prefill_unit
+
+
 def _project_no_transpose(k_pre_b, B_b, storage=None):
     B = np.asarray(B_b, np.float64)
     H, r, d = B.shape
@@ -123,6 +130,7 @@ MUTANTS = [
     ("project_new_key", _project_first_head_only, [pins.test_plus_projection_closed_form_in_span,
                                                    pins.test_plus_projection_brute_force]),
     ("new_token_key", _new_key_without_rope, [pins.test_plus_full_rank_equals_exact_new_keys]),
+    ("prefill_unit", _prefill_ignores_exact_keys, [pins.test_exact_key_prefill_brute_force]),
 ]
 
 

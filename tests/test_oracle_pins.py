@@ -446,3 +446,60 @@ def test_plus_full_rank_equals_exact_new_keys():
             r2 = ref.decode_step_unit(st_plus, qg, k_plus, c["vn"][t, h], A, B[h], c["V"][h], 6, c["C"], base)
             assert np.array_equal(r1["sel"], r2["sel"])
             np.testing.assert_allclose(r2["out"], r1["out"], rtol=0, atol=1e-11)
+
+
+# --------------------------------------------------------------------- exact-key pre-filling
+
+
+def test_exact_key_prefill_brute_force():
+    """Landmarks, min-cos, outliers and kept keys come from RoPE(K_exact), not A.B:
+    checked against loops with an independent RoPE on keys unrelated to the factors."""
+    rng = np.random.default_rng(51)
+    S, C, W, O, d, r, base = 64, 8, 8, 2, 8, 4, 10000.0
+    K = rng.standard_normal((S, d))
+    K[3 * C + 1] *= 9.0                                  # one token far from its chunk mean
+    A = rng.standard_normal((S, r))
+    B = rng.standard_normal((r, d))
+    V = rng.standard_normal((S, d))
+    pre = ref.prefill_unit(A, B, V, C, O, W, base, K_exact=K)
+    Kr = _rope_complex(K, np.arange(S), base)
+    n_cand = S // C - W // C
+    mc = np.empty(n_cand)
+    for c in range(n_cand):
+        mean = Kr[c * C:(c + 1) * C].mean(axis=0)
+        np.testing.assert_allclose(pre.all_landmarks[c], mean, rtol=0, atol=1e-12)
+        mc[c] = min(float(Kr[i] @ mean) / max(np.linalg.norm(Kr[i]) * np.linalg.norm(mean), 1e-12)
+                    for i in range(c * C, (c + 1) * C))
+    np.testing.assert_allclose(pre.min_cos, mc, rtol=0, atol=1e-12)
+    want_out = sorted(sorted(range(n_cand), key=lambda c: (mc[c], c))[:O])
+    assert list(pre.outlier_ids) == want_out and 3 in want_out
+    tok = ref.chunk_tokens(pre.outlier_ids, C)
+    np.testing.assert_allclose(pre.k_outlier, Kr[tok], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(np.stack(pre.k_local), Kr[S - W:], rtol=0, atol=1e-12)
+
+
+def test_exact_keys_equal_to_the_factors_change_nothing():
+    c = _dense_case(seed=52, steps=1)
+    base, h = 500000.0, 1
+    a = ref.prefill_unit(c["A"], c["Bs"][h], c["V"][h], c["C"], c["O"], c["W"], base)
+    b = ref.prefill_unit(c["A"], c["Bs"][h], c["V"][h], c["C"], c["O"], c["W"], base,
+                         K_exact=c["A"] @ c["Bs"][h])
+    np.testing.assert_allclose(b.all_landmarks, a.all_landmarks, rtol=0, atol=1e-12)
+    assert np.array_equal(a.outlier_ids, b.outlier_ids)
+
+
+def test_attend_with_exact_outlier_keys_matches_decode_step():
+    rng = np.random.default_rng(53)
+    c = _dense_case(seed=53, steps=2)
+    base, h, K = 500000.0, 0, 5
+    Kx = c["A"] @ c["Bs"][h] + 0.3 * rng.standard_normal((c["S"], c["d"]))
+    st = ref.UnitDecodeState(ref.prefill_unit(c["A"], c["Bs"][h], c["V"][h], c["C"], c["O"], c["W"], base,
+                                              K_exact=Kx))
+    for t in range(2):
+        qg = c["qs"][t, h * c["G"]:(h + 1) * c["G"]]
+        res = ref.decode_step_unit(st, qg, c["kn"][t, h], c["vn"][t, h], c["A"], c["Bs"][h],
+                                   c["V"][h], K, c["C"], base)
+        again = ref.attend_on_index_set(qg, c["A"], c["Bs"][h], c["V"][h], st.pre.outlier_ids,
+                                        res["sel"], st.pre.k_local, st.pre.v_local, c["C"], base,
+                                        k_outlier=st.pre.k_outlier)
+        np.testing.assert_allclose(again, res["out"], rtol=0, atol=1e-13)

@@ -14,6 +14,7 @@ here.  The recipe (one seeded torch generator per layer and purpose):
   Gaussian matrix), and A is scaled by sqrt(H*d/r) so that the keys keep unit
   per-coordinate variance.
 * V [b][H][S][d] ~ N(0,1).
+* exact pre-RoPE keys (pre-filling from exact keys only): A.B_h + N(0, 0.01).
 * queries q [T][b][H*G][d]: q_0 ~ N(0,1), q_t = drift*q_{t-1} + sqrt(1-drift^2)*eps
   (already post-RoPE, as a model hands them to the attention).
 * new tokens k_new, v_new [T][b][H][d] ~ N(0,1): the key of a generated token
@@ -34,7 +35,7 @@ import torch
 
 from .configs import Workload
 
-_PURPOSE = {"A": 1, "spike": 2, "B": 3, "V": 4, "q": 5, "k_new": 6, "v_new": 7}
+_PURPOSE = {"A": 1, "spike": 2, "B": 3, "V": 4, "q": 5, "k_new": 6, "v_new": 7, "k_exact": 8}
 
 
 def _gen(w: Workload, layer: int, purpose: str, device) -> torch.Generator:
@@ -111,6 +112,22 @@ def make_B(w: Workload, layer: int, device="cpu") -> torch.Tensor:
     B = torch.randn((w.batch, w.n_kv_heads, w.rank, w.head_dim), generator=g, device=device,
                     dtype=torch.float32) / math.sqrt(w.rank)
     return B.to(storage_dtype(w))
+
+
+def make_K_exact(w: Workload, layer: int, device="cpu", A=None, B=None) -> torch.Tensor:
+    """Exact pre-RoPE keys [b][H][S][d] for pre-filling from exact keys: the
+    factors' keys A.B_h plus N(0, 0.01) noise (the configs' noisy keys), so the
+    factors are a close but not exact low-rank fit of them."""
+    A = make_A(w, layer, device) if A is None else A
+    B = make_B(w, layer, device) if B is None else B
+    g = _gen(w, layer, "k_exact", device)
+    K = torch.empty((w.batch, w.n_kv_heads, w.seq_len, w.head_dim), dtype=storage_dtype(w), device=device)
+    for b in range(w.batch):
+        Af = A[b].float()
+        for h in range(w.n_kv_heads):
+            noise = torch.randn((w.seq_len, w.head_dim), generator=g, device=device, dtype=torch.float32)
+            K[b, h] = (Af @ B[b, h].float() + 0.1 * noise).to(K.dtype)
+    return K
 
 
 def make_V(w: Workload, layer: int, device="cpu") -> torch.Tensor:
