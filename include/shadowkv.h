@@ -130,6 +130,21 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
                            skv_stream stream, skv_layer** out);
 
 /*
+ * Algorithm 1 as the digest states it (section A2): its inputs are the exact
+ * keys K and K_RoPE, and the landmarks, the min-cosine outlier test, the
+ * outlier keys and the local window's keys are built from K_RoPE = RoPE(K),
+ * while A and B (the SVD of K, computed by the caller) serve only the sparse
+ * reconstruction at decode time.
+ *
+ *   K  dev [b][H][S][d]  exact pre-RoPE keys, storage dtype (bf16; fp32 for
+ *      SKV_F32; bf16 for SKV_FP8), 16-byte aligned.  Read during this call
+ *      only: the library keeps no reference to it.
+ * Everything else as shadowkv_prefill_index; K = NULL is that call.
+ */
+int shadowkv_prefill_index_keys(const skv_config* cfg, const void* A, const void* B, const void* K,
+                                const void* V, skv_stream stream, skv_layer** out);
+
+/*
  * Algorithm 2 (decoding), one step of one layer:
  *   1. appends (k_new, v_new) to the exact local set;
  *   2. P = q.L^T for the G query heads of every KV head (q-head j belongs to

@@ -24,7 +24,8 @@ FIELDS = {
 NEW_KEYS = {"exact": 0, "lowrank": 1}
 ERRORS = {0: "OK", -1: "INVALID", -2: "OOM", -3: "NOT_PINNED", -4: "CUDA", -5: "DEVICE_BOUNDS",
           -6: "TIMEOUT", -7: "STEP_LIMIT", -8: "UNSUPPORTED"}
-EXPORTED = ("shadowkv_validate_config", "shadowkv_prefill_index", "shadowkv_decode_step",
+EXPORTED = ("shadowkv_validate_config", "shadowkv_prefill_index", "shadowkv_prefill_index_keys",
+            "shadowkv_decode_step",
             "shadowkv_stats", "shadowkv_reset_stats", "shadowkv_set_profiling",
             "shadowkv_export_size", "shadowkv_export", "shadowkv_model", "shadowkv_destroy",
             "shadowkv_strerror", "shadowkv_version", "shadowkv_host_alloc", "shadowkv_host_free",
@@ -88,6 +89,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
     lib.shadowkv_validate_config.argtypes = [ctypes.POINTER(SkvConfig)]
     lib.shadowkv_prefill_index.argtypes = [ctypes.POINTER(SkvConfig), vp, vp, vp, vp, ctypes.POINTER(vp)]
+    lib.shadowkv_prefill_index_keys.argtypes = [ctypes.POINTER(SkvConfig), vp, vp, vp, vp, vp, ctypes.POINTER(vp)]
     lib.shadowkv_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
     lib.shadowkv_stats.argtypes = [vp, ctypes.POINTER(SkvStats)]
     lib.shadowkv_reset_stats.argtypes = [vp]
@@ -220,13 +222,19 @@ class HostBuffer:
 class Layer:
     """One layer's ShadowKV state (the handle of shadowkv_prefill_index)."""
 
-    def __init__(self, cfg: SkvConfig, A, B, V, stream=None):
+    def __init__(self, cfg: SkvConfig, A, B, V, stream=None, K=None):
+        """K: optional exact pre-RoPE keys [b][H][S][d] (pre-filling from exact keys)."""
         lib = load()
         self.cfg = cfg
         self._keep = (A, B, V)   # the library borrows these
         h = ctypes.c_void_p()
-        _check(lib.shadowkv_prefill_index(ctypes.byref(cfg), _ptr(A), _ptr(B), _ptr(V), _stream(stream),
-                                          ctypes.byref(h)), "shadowkv_prefill_index")
+        if K is None:
+            _check(lib.shadowkv_prefill_index(ctypes.byref(cfg), _ptr(A), _ptr(B), _ptr(V), _stream(stream),
+                                              ctypes.byref(h)), "shadowkv_prefill_index")
+        else:
+            _check(lib.shadowkv_prefill_index_keys(ctypes.byref(cfg), _ptr(A), _ptr(B), _ptr(K), _ptr(V),
+                                                   _stream(stream), ctypes.byref(h)),
+                   "shadowkv_prefill_index_keys")
         self._h = h
 
     @property

@@ -288,12 +288,18 @@ int shadowkv_model(const skv_config* c, double alpha, int64_t t, double b_gpu_gb
 
 int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, const void* V, skv_stream stream,
                            skv_layer** out) {
+    return shadowkv_prefill_index_keys(cfg, A, B, nullptr, V, stream, out);
+}
+
+int shadowkv_prefill_index_keys(const skv_config* cfg, const void* A, const void* B, const void* Kx, const void* V,
+                                skv_stream stream, skv_layer** out) {
     if (!out) return SKV_ERR_INVALID;
     *out = nullptr;
     int rc = shadowkv_validate_config(cfg);
     if (rc) return rc;
     if (!A || !B || !V) return SKV_ERR_INVALID;
-    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(V)) & 15)
+    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(V) |
+         reinterpret_cast<uintptr_t>(Kx)) & 15)
         return SKV_ERR_INVALID;
     cudaStream_t s = stream;
     skv_layer* h = new (std::nothrow) skv_layer();
@@ -339,7 +345,7 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
     h->A = A;
     h->B = B;
     h->V = V;
-    if (!is_device_ptr(A) || !is_device_ptr(B)) return fail(SKV_ERR_INVALID);
+    if (!is_device_ptr(A) || !is_device_ptr(B) || (Kx && !is_device_ptr(Kx))) return fail(SKV_ERR_INVALID);
     if (c.v_place == SKV_V_HBM) {
         if (!is_device_ptr(V)) return fail(SKV_ERR_INVALID);
         h->Vd = V;
@@ -471,9 +477,12 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
     rp.U = U; rp.H = h->H; rp.r = h->r; rp.nkb = h->nkb; rp.S = h->S; rp.nchunk = h->nchunk;
     rp.rope_lo = h->rope_lo; rp.rope_hi = h->rope_hi; rp.nhi = h->nhi;
     rp.A = A; rp.B = B; rp.err = h->err;
+    rp.Kx = Kx; rp.kx_es = h->es;
+    // K_RoPE: the exact keys' rotation when the caller has them, else the factors' keys
     auto rebuild = [&](const RebuildParams& p, int count_max) -> int {
         const int gx = (count_max + kTileChunks - 1) / kTileChunks;
         if (gx <= 0) return 0;
+        if (Kx) return launch_keys_exact(p, gx, h->dtype != SKV_F32, s);
         return h->tc ? launch_rebuild_tc(&h->tmA, &h->tmB, p, gx, s) : launch_rebuild_f32(p, gx, s);
     };
     // 1. landmarks and min-cos of every candidate chunk (Algorithm 1: Reduce, CosineSimilarity, Min)

@@ -346,6 +346,69 @@ __global__ void __launch_bounds__(128) k_rebuild_f32(RebuildParams p) {
     }
 }
 
+// ------------------------------------------------------------------ exact keys (pre-filling)
+// Algorithm 1 of the digest (section A2) takes the exact keys K and K_RoPE and
+// builds the landmarks, the min-cosine test and the outlier keys from K_RoPE.
+// When the caller has K, the tile's rows are the exact pre-RoPE keys, read
+// straight into the fp32 staging tile (warp w loads rows w, w+4, ..., lane l
+// dims [4l, 4l+4)); RoPE and the statistics follow as for rebuilt rows.
+template <typename InT, typename OutT>
+__global__ void __launch_bounds__(128) k_keys_exact(RebuildParams p) {
+    extern __shared__ __align__(16) uint8_t smem_x[];
+    __shared__ TileInfo ti[kTileChunks];
+    const int u = blockIdx.y, tile = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nch = load_tile_info(p, u, tile, ti);
+    if (nch == 0) return;
+    float* stage = reinterpret_cast<float*>(smem_x);               // [128][pitch]
+    float* smean = stage + kRows * kStagePitch;                    // [16][d]
+    __syncthreads();
+    const InT* K = static_cast<const InT*>(p.Kx) + static_cast<int64_t>(u) * p.S * kD;
+    for (int row = warp; row < kRows; row += 4) {
+        const TileInfo t = ti[row >> 3];
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t.chunk >= 0) {
+            const InT* src = K + (static_cast<int64_t>(t.chunk) * kC + (row & 7)) * kD + 4 * lane;
+            if constexpr (sizeof(InT) == 2) {
+                const uint2 w = *reinterpret_cast<const uint2*>(src);
+                const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
+                const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
+                v = make_float4(a.x, a.y, b.x, b.y);
+            } else {
+                v = *reinterpret_cast<const float4*>(src);
+            }
+        }
+        *reinterpret_cast<float4*>(stage + row * kStagePitch + 4 * lane) = v;
+    }
+    __syncthreads();
+    RopeRegs first;
+    rope_fetch(p, ti[warp], first);
+    rope_tile<OutT>(p, u, ti, stage, first);
+    if (p.mode == 1) {
+        __syncthreads();
+        tile_stats(p, u, ti, stage, smean);
+    }
+}
+
+int launch_keys_exact(const RebuildParams& p, int grid_x, bool out_bf16, cudaStream_t s) {
+    const size_t smem = static_cast<size_t>(kRows * kStagePitch + kTileChunks * kD) * sizeof(float);
+    const dim3 grid(grid_x, p.U);
+    cudaError_t e;
+    if (p.kx_es == 2) {
+        if (!out_bf16) return -1;
+        auto k = k_keys_exact<__nv_bfloat16, __nv_bfloat16>;
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        k<<<grid, 128, smem, s>>>(p);
+        e = cudaGetLastError();
+    } else {
+        if (out_bf16) return -1;
+        auto k = k_keys_exact<float, float>;
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        k<<<grid, 128, smem, s>>>(p);
+        e = cudaGetLastError();
+    }
+    return e == cudaSuccess ? 0 : -1;
+}
+
 // ------------------------------------------------------------------ ShadowKV+ projection
 // The rank-r state of a generated token (summary page, "The ShadowKV+ extension
 // for generated tokens"): a[j] = sum over heads h and dims i of k'[h][i] * B[h][j][i],

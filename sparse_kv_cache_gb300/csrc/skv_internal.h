@@ -101,6 +101,8 @@ struct RebuildParams {
     const float2* rope_lo;    // [256][d/2] (cos, sin) of lo * theta_i
     const float2* rope_hi;    // [nhi][d/2] (cos, sin) of hi * 256 * theta_i
     int nhi;
+    const void* Kx;           // exact pre-RoPE keys [U][S][d] (pre-filling from exact keys), or NULL
+    int kx_es;                // their element size: 2 (bf16) or 4 (fp32)
     const void* A;            // fp32 path: [b][S][r]
     const void* B;            // fp32 path: [U][r][d]
     int* err;
@@ -108,6 +110,8 @@ struct RebuildParams {
 int launch_rebuild_tc(const CUtensorMap* tmA, const CUtensorMap* tmB, const RebuildParams& p, int grid_x,
                       cudaStream_t s);
 int launch_rebuild_f32(const RebuildParams& p, int grid_x, cudaStream_t s);
+// the same outputs from exact pre-RoPE keys p.Kx instead of A.B (keys stored as bf16 when out_bf16)
+int launch_keys_exact(const RebuildParams& p, int grid_x, bool out_bf16, cudaStream_t s);
 int launch_transpose_B(const void* B, void* Bt, int U, int r, cudaStream_t s);
 // ShadowKV+: a[b] = k'[b] . B_b^T (k' [b][H][d], B [b][H][r][d]) into row t of a_new [b][a_rows][r]
 int launch_project(int dtype, const void* k_new, const void* B, void* a_new, int batch, int H, int r,

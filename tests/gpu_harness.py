@@ -13,7 +13,7 @@ import torch
 
 import sparse_kv_cache_gb300 as skv
 from oracle import shadowkv_ref as ref
-from workload import Workload, make_A, make_B, make_decode_inputs, make_V
+from workload import Workload, make_A, make_B, make_decode_inputs, make_K_exact, make_V
 
 
 def np64(t: torch.Tensor) -> np.ndarray:
@@ -47,11 +47,13 @@ class LayerRun:
     """One layer on the GPU plus lazily computed oracle state per unit."""
 
     def __init__(self, w: Workload, steps: int, gen_device: str = "cpu", layer: int = 0,
-                 side_stream: bool = True, host_alloc: str = "pinned"):
+                 side_stream: bool = True, host_alloc: str = "pinned", exact_keys: bool = False):
         self.w, self.steps = w, steps
         dev = torch.device("cuda")
         A = make_A(w, layer, gen_device)
         B = make_B(w, layer, gen_device)
+        # pre-filling from exact keys: the library reads them during prefill only
+        self.K_src = make_K_exact(w, layer, gen_device, A, B) if exact_keys else None
         V = make_V(w, layer, gen_device)
         q, kn, vn = make_decode_inputs(w, layer, steps, gen_device)
         self.A_d, self.B_d = A.to(dev), B.to(dev)
@@ -73,7 +75,8 @@ class LayerRun:
         self.cfg = skv.make_config(w, max_new_tokens=steps)
         self.main = torch.cuda.Stream()
         self.side = torch.cuda.Stream(priority=-10) if side_stream else None
-        self.layer = skv.Layer(self.cfg, self.A_d, self.B_d, self.V_arg, stream=self.main)
+        self.layer = skv.Layer(self.cfg, self.A_d, self.B_d, self.V_arg, stream=self.main,
+                               K=None if self.K_src is None else self.K_src.to(dev))
         self.U, self.G, self.K = w.units, w.group, w.n_select
         self.out = torch.empty((w.batch, w.n_q_heads, w.head_dim), dtype=self.q_d.dtype, device=dev)
         self.sel = torch.empty((w.batch, w.n_kv_heads, w.n_select), dtype=torch.int32, device=dev)
@@ -115,8 +118,12 @@ class LayerRun:
         if u not in self._pre:
             A, B, V = self.unit_inputs(u)
             w = self.w
-            self._pre[u] = (ref.prefill_unit(A, B, V, w.chunk, w.n_outlier, w.local_window, w.rope_base),
-                            A, B, V)
+            Kx = None
+            if self.K_src is not None:
+                b, h = divmod(u, w.n_kv_heads)
+                Kx = np64(self.K_src[b, h])
+            self._pre[u] = (ref.prefill_unit(A, B, V, w.chunk, w.n_outlier, w.local_window, w.rope_base,
+                                             K_exact=Kx), A, B, V)
         return self._pre[u][0]
 
     # ------------------------------------------------------------ steps
@@ -179,11 +186,11 @@ def check_prefill(run: LayerRun, units) -> dict:
         # outlier chunks' keys and values
         if O:
             tok = ref.chunk_tokens(oid[u], C)
-            Ko = ref.rebuild_keys(A[tok], B, tok, w.rope_base)
+            Ko = _context_keys(run, u, A, B, tok)
             _close_keys(kout[u], Ko, kd, "k_outlier")
             assert np.array_equal(vout[u], V[tok]), "v_outlier"
         # local window
-        Kl = ref.rebuild_keys(A[w.seq_len - W:], B, np.arange(w.seq_len - W, w.seq_len), w.rope_base)
+        Kl = _context_keys(run, u, A, B, np.arange(w.seq_len - W, w.seq_len))
         _close_keys(kloc[u][:W], Kl, kd, "k_local")
         assert np.array_equal(vloc[u][:W], V[w.seq_len - W:]), "v_local"
     return {"outlier_near_ties": ties}
@@ -267,9 +274,10 @@ def check_step(run: LayerRun, units, rep: Report, prev_sel: dict, check_cache: b
         kl = [pre_row for pre_row in _local_keys(run, u, A, B)] + [_new_key(run, s, b, h) for s in range(t + 1)]
         vl = list(V[w.seq_len - W:]) + [np64(run.vn_src[s, b, h]) for s in range(t + 1)]
         oo = oid[u] if oid is not None else []
+        ko = _context_keys(run, u, A, B, ref.chunk_tokens(oo, C)) if run.K_src is not None else None
         want = ref.attend_on_index_set(q[u], A, B, V, oo, sel[u], kl, vl, C, w.rope_base, storage=kd,
-                                       v_storage=ref.value_storage(w.dtype))
-        exact = ref.attend_on_index_set(q[u], A, B, V, oo, sel[u], kl, vl, C, w.rope_base)
+                                       v_storage=ref.value_storage(w.dtype), k_outlier=ko)
+        exact = ref.attend_on_index_set(q[u], A, B, V, oo, sel[u], kl, vl, C, w.rope_base, k_outlier=ko)
         err = np.max(np.abs(out[u] - want))
         rel = err / max(np.max(np.abs(want)), 1e-30)
         rep.max_out_err = max(rep.max_out_err, err)
@@ -308,18 +316,30 @@ def check_new_states(run: LayerRun, rep_err: list):
             rep_err.append(float(err.max()))
 
 
+def _context_keys(run: LayerRun, u: int, A, B, tok) -> np.ndarray:
+    """K_RoPE of context tokens as pre-filling keeps them: the rotated exact keys
+    when pre-filling had them, else the factors' keys."""
+    w = run.w
+    tok = np.asarray(tok, dtype=np.int64)
+    if run.K_src is None:
+        return ref.rebuild_keys(A[tok], B, tok, w.rope_base)
+    b, h = divmod(u, w.n_kv_heads)
+    return ref.apply_rope(np64(run.K_src[b, h])[tok], tok, w.rope_base)
+
+
 def _local_keys(run: LayerRun, u: int, A, B):
     w = run.w
     W = w.local_window
     if W == 0:
         return []
     pos = np.arange(w.seq_len - W, w.seq_len)
-    return list(ref.rebuild_keys(A[pos], B, pos, w.rope_base))
+    return list(_context_keys(run, u, A, B, pos))
 
 
 def run_and_check(w: Workload, steps: int, units=None, gen_device="cpu", check_cache=True,
-                  side_stream=True, host_alloc="pinned") -> Report:
-    run = LayerRun(w, steps, gen_device=gen_device, side_stream=side_stream, host_alloc=host_alloc)
+                  side_stream=True, host_alloc="pinned", exact_keys=False) -> Report:
+    run = LayerRun(w, steps, gen_device=gen_device, side_stream=side_stream, host_alloc=host_alloc,
+                   exact_keys=exact_keys)
     units = list(range(w.units)) if units is None else list(units)
     check_prefill(run, units)
     rep = Report()
