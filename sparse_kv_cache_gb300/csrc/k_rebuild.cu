@@ -108,11 +108,13 @@ __device__ __forceinline__ void rope_chunk(const RebuildParams& p, int u, int c,
 template <typename OutT>
 __device__ void rope_tile(const RebuildParams& p, int u, const TileInfo* ti, float* stage, const RopeRegs& first) {
     const int warp = threadIdx.x >> 5;
-    rope_chunk<OutT>(p, u, warp, ti[warp], first, stage);
-    for (int c = warp + 4; c < kTileChunks; c += 4) {
-        RopeRegs r;
-        rope_fetch(p, ti[c], r);
-        rope_chunk<OutT>(p, u, c, ti[c], r, stage);
+    // the next chunk's table entries are in flight while the current chunk rotates
+    RopeRegs cur = first;
+    for (int c = warp; c < kTileChunks; c += 4) {
+        RopeRegs nxt;
+        if (c + 4 < kTileChunks) rope_fetch(p, ti[c + 4], nxt);
+        rope_chunk<OutT>(p, u, c, ti[c], cur, stage);
+        cur = nxt;
     }
 }
 
@@ -198,9 +200,24 @@ __global__ void __launch_bounds__(128, 1) k_rebuild_tc(const __grid_constant__ C
     __shared__ TileInfo ti[kTileChunks];
     __shared__ int s_fail;
 
-    const int u = blockIdx.y, tile = blockIdx.x, tid = threadIdx.x, warp = tid >> 5;
-    const int nch = load_tile_info(p, u, tile, ti);
-    if (nch == 0) return;   // uniform: every thread computed the same count
+    // units along x, tiles along y: the first tiles of every unit are dispatched before any
+    // unit's later (often empty) ones
+    const int u = blockIdx.x, tile = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
+    // the list entries are read in the same round trip as the count (in bounds up to list_cap)
+    int ch_raw = 0, dst_raw = 0;
+    const int first_idx = tile * kTileChunks;
+    if (tid < kTileChunks && first_idx + tid < p.list_cap) {
+        const int idx = first_idx + tid;
+        ch_raw = p.list ? p.list[u * p.list_us + idx] : p.list_base + idx;
+        dst_raw = p.dst_idx ? p.dst_idx[u * p.list_us + idx] : idx;
+    }
+    int count = p.cnt ? p.cnt[u] : p.count_const;
+    if (count < 0 || count > p.list_cap) {
+        if (tid == 0) set_err(p.err, DEV_ERR_BOUNDS, 401);
+        count = 0;
+    }
+    if (first_idx >= count) return;   // uniform
+    const int nch = min(kTileChunks, count - first_idx);
     const int nkb = p.nkb;
     uint8_t* sA = smem;                      // nkb x [128 rows][128 B]
     uint8_t* sB = smem + nkb * 16384;        // nkb x [128 rows][128 B]
@@ -211,6 +228,23 @@ __global__ void __launch_bounds__(128, 1) k_rebuild_tc(const __grid_constant__ C
         fence_mbar_init();
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+        // the unit's B slice does not depend on the chunk list: in flight while the list is read
+        mbar_expect_tx(&bar_tma, static_cast<uint32_t>(nkb * 16384));
+        for (int kb = 0; kb < nkb; ++kb) tma_load_2d(sB + kb * 16384, &tmB, kb * 64, u * kD, &bar_tma);
+    }
+    if (tid < kTileChunks) {
+        TileInfo t{-1, 0};
+        if (tid < nch) {
+            const int ch = ch_raw, dst = dst_raw;
+            if (ch < 0 || ch >= p.nchunk || (p.mode == 0 && (dst < 0 || dst >= p.dst_cap)) ||
+                (p.mode == 1 && ch >= p.stats_us)) {
+                set_err(p.err, DEV_ERR_BOUNDS, 402);
+            } else {
+                t.chunk = ch;
+                t.dst = dst;
+            }
+        }
+        ti[tid] = t;
     }
     if (warp == 0) {
         tmem_alloc(&tmem_slot, 128);
@@ -222,17 +256,15 @@ __global__ void __launch_bounds__(128, 1) k_rebuild_tc(const __grid_constant__ C
     const uint32_t tmem = tmem_slot;
     const int b = u / p.H;
 
+    // A rows: one issuing thread per chunk (its nkb 64-column boxes of 8 rows)
+    if (tid < nch && ti[tid].chunk >= 0)
+        for (int kb = 0; kb < nkb; ++kb)
+            tma_load_2d(sA + kb * 16384 + tid * 1024, &tmA, kb * 64,
+                        static_cast<int>(b * p.S + static_cast<int64_t>(ti[tid].chunk) * kC), &bar_tma);
     if (tid == 0) {
         int nvalid = 0;
         for (int c = 0; c < nch; ++c) nvalid += ti[c].chunk >= 0;
-        mbar_arrive_expect_tx(&bar_tma, static_cast<uint32_t>(nkb * (16384 + nvalid * 1024)));
-        for (int kb = 0; kb < nkb; ++kb) {
-            tma_load_2d(sB + kb * 16384, &tmB, kb * 64, u * kD, &bar_tma);
-            for (int c = 0; c < nch; ++c)
-                if (ti[c].chunk >= 0)
-                    tma_load_2d(sA + kb * 16384 + c * 1024, &tmA, kb * 64,
-                                static_cast<int>(b * p.S + static_cast<int64_t>(ti[c].chunk) * kC), &bar_tma);
-        }
+        mbar_arrive_expect_tx(&bar_tma, static_cast<uint32_t>(nkb * nvalid * 1024));
         if (!mbar_wait(&bar_tma, 0)) {
             set_err(p.err, DEV_ERR_TIMEOUT, 411);
             (void)mbar_wait(&bar_tma, 0);
@@ -481,7 +513,7 @@ int launch_rebuild_tc(const CUtensorMap* tmA, const CUtensorMap* tmB, const Rebu
     const size_t smem = tc_smem(p);
     auto fn = k_rebuild_tc<__nv_bfloat16>;
     cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    fn<<<dim3(grid_x, p.U), 128, smem, s>>>(*tmA, *tmB, p);
+    fn<<<dim3(p.U, grid_x), 128, smem, s>>>(*tmA, *tmB, p);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
