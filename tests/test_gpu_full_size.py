@@ -26,3 +26,21 @@ def test_llama_1m_b1_host_values():
 def test_sweep_64k_b48_host_values():
     w = SWEEP_64K.with_(batch=48, v_place="host", drift=0.5)
     run_and_check(w, 2, units=[0, 200, 383], gen_device="cuda", check_cache=False)
+
+
+def test_llama_128k_b8_fp8_host_values():
+    """The e5m2 configuration at the benchmark's 128K size (bench.py --dtype fp8)."""
+    rep = run_and_check(LLAMA_128K.with_(dtype="fp8"), 3, units=[1, 38, 62], gen_device="cuda",
+                        check_cache=False, host_alloc="arena")
+    assert rep.steps == 3
+
+
+def test_llama_128k_b8_lowrank_new_keys():
+    """ShadowKV+ at the benchmark's 128K size (bench.py --new-keys lowrank), values in HBM."""
+    run_and_check(LLAMA_128K.with_(new_keys="lowrank", v_place="hbm"), 10, units=[2, 40, 63],
+                  gen_device="cuda", check_cache=False)
+
+
+def test_llama_32k_b4_exact_keys():
+    """Pre-filling from exact keys at the 32K b4 size."""
+    run_and_check(LLAMA_32K, 3, units=[0, 17, 31], gen_device="cuda", check_cache=True, exact_keys=True)
