@@ -30,10 +30,10 @@ sys.path.insert(0, ROOT)
 from workload import ALL, LLAMA_128K, Workload  # noqa: E402
 
 # DRAM traffic of one k_score_tc launch from an ncu capture (dram__bytes_read.sum +
-# dram__bytes_write.sum = 133.89 + 4.65 MB over 32 units at 128K, bf16), valid only while
+# dram__bytes_write.sum = 133.89 + 4.35 MB over 32 units at 128K, bf16), valid only while
 # the scorer source is the one that was profiled; per unit, scaled to a launch by its units.
-SCORE_TRAFFIC = {"source_sha256": "1f96b4682ac28cf2c31680e6d4c4a093f1f6990af7e78e3803252981285f75fb",
-                 "seq_len": 131072, "dtype": "bf16", "bytes_per_unit": (133892096 + 4653568) / 32}
+SCORE_TRAFFIC = {"source_sha256": "6b81a89c450e7c0b18c603f24db0192aae24ae37004b7445e69bd0cdc73c951f",
+                 "seq_len": 131072, "dtype": "bf16", "bytes_per_unit": (133885696 + 4347136) / 32}
 
 # kernels one layer's decode step launches: score, select, gather, rebuild, attention, merge;
 # the e5m2 configuration adds the query split ahead of the scorer; ShadowKV+ adds the projection
