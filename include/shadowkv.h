@@ -192,6 +192,7 @@ typedef struct {
     double  phase_ms[SKV_NPHASE];        /* summed event time per phase (profiling) */
     int64_t phase_launches[SKV_NPHASE];  /* launches timed per phase */
     int32_t device_error;       /* 0, SKV_ERR_DEVICE_BOUNDS or SKV_ERR_TIMEOUT */
+    int64_t kernel_launches;    /* kernels the decode steps launched since the last reset */
 } skv_stats;
 
 /*

@@ -50,7 +50,7 @@ class SkvStats(ctypes.Structure):
                 ("hbm_bytes", ctypes.c_double), ("link_bytes", ctypes.c_double),
                 ("scratch_bytes", ctypes.c_double),
                 ("phase_ms", ctypes.c_double * 5), ("phase_launches", ctypes.c_int64 * 5),
-                ("device_error", ctypes.c_int32)]
+                ("device_error", ctypes.c_int32), ("kernel_launches", ctypes.c_int64)]
 
 
 class SkvAttentionArgs(ctypes.Structure):

@@ -78,6 +78,7 @@ struct skv_layer {
     CUtensorMap tmKall{};                 // the key blocks, [U*R][128], 128-row boxes (attention)
     int score_ncta = 0, score_nru = 0, score_nparts = 0, sel_smem_cap = 0;
     int32_t* sched = nullptr;
+    int64_t launches = 0;                 // kernels launched by decode steps since the last reset
     int newkeys = SKV_NEWKEYS_EXACT;
     int Tpad = 0;                         // max_new_tokens rounded up to whole chunks
     void* Anew = nullptr;                 // ShadowKV+: rank-r states of generated tokens, [b][Tpad][r]
@@ -643,9 +644,11 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     ap.nsplit = (ap.n_out + ap.n_cache + ap.n_loc + seg - 1) / seg;
     ap.scale = sp.scale; ap.G = G; ap.U = U; ap.err = h->err;
     ap.v_es = h->es_v;
-    if (h->tc ? launch_attn_tc(&h->tmKall, ap, h->sm_count, sm)
-                             : launch_attn(h->dtype, ap, sm))
-        return SKV_ERR_CUDA;
+    const int na = h->tc ? launch_attn_tc(&h->tmKall, ap, h->sm_count, sm) : (launch_attn(h->dtype, ap, sm) ? -1 : 1);
+    if (na < 0) return SKV_ERR_CUDA;
+    // score, select, fetch, rebuild, attention (+ its merge); the e5m2 query split; ShadowKV+'s
+    // projection and generated-key rebuild
+    h->launches += 4 + na + (h->dtype == SKV_FP8 ? 1 : 0) + (h->newkeys == SKV_NEWKEYS_LOWRANK ? 2 : 0);
     if (h->profiling) {
         cudaEventRecord(ev[4], sm);
         h->prof_pending.push_back(ev);
@@ -710,6 +713,7 @@ int shadowkv_stats(skv_layer* h, skv_stats* out) {
     }
     const int e = check_device_error(h);
     out->device_error = (e == SKV_ERR_DEVICE_BOUNDS || e == SKV_ERR_TIMEOUT) ? e : 0;
+    out->kernel_launches = h->launches;
     return e;
 }
 
@@ -718,6 +722,7 @@ int shadowkv_reset_stats(skv_layer* h) {
     skv_stats tmp;
     shadowkv_stats(h, &tmp);
     h->t_reset = h->t;
+    h->launches = 0;
     for (int ph = 0; ph < SKV_NPHASE; ++ph) { h->phase_ms[ph] = 0; h->phase_n[ph] = 0; }
     return SKV_OK;
 }

@@ -784,7 +784,7 @@ static int launch_tc(const CUtensorMap* tmK, const AttnParams& p, int nsm, cudaS
         return -1;
     const int64_t F = static_cast<int64_t>(p.U) * p.nsplit;
     const int ncta = static_cast<int>(F < nsm ? F : nsm);
-    if (ncta <= 0) return 0;
+    if (ncta <= 0) return -1;
     if (F * (ncta + 1) > INT32_MAX || static_cast<int64_t>(p.U) * p.unit_rows > INT32_MAX) return -1;   // 32-bit indexing
     const size_t smem = static_cast<size_t>(AStages<G>::value) * kAStage + static_cast<size_t>(4) * G * kD * 4 + 1024;
     cudaFuncSetAttribute(k_attn_tc<G, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -804,7 +804,7 @@ static int launch_tc(const CUtensorMap* tmK, const AttnParams& p, int nsm, cudaS
         cudaGetLastError();
         return -1;
     }
-    return 0;
+    return 2;   // the attention kernel and its merge
 }
 
 int launch_attn_tc(const CUtensorMap* k_all, const AttnParams& p, int nsm, cudaStream_t s) {

@@ -156,7 +156,7 @@ int launch_attn(int dtype, const AttnParams& p, cudaStream_t s);
 // bf16: persistent tensor-core form, one CTA per SM (nsm), nsplit = ceil(tokens / 128); needs the
 // block layout (unit_rows > 0, regions adjacent in each block) and a tensor map over the key
 // blocks, [U * unit_rows][128] (box 64 x 128, 128-byte swizzle)
-int launch_attn_tc(const CUtensorMap* k_all, const AttnParams& p, int nsm, cudaStream_t s);
+int launch_attn_tc(const CUtensorMap* k_all, const AttnParams& p, int nsm, cudaStream_t s);   // kernels launched, or -1
 int attn_segment(int dtype);   // tokens per attention CTA
 
 }  // namespace skv
