@@ -129,8 +129,9 @@ def test_model_reproduces_pages_example(lib):
     assert abs(m["memory_savings"] - 7.08) < 0.005
 
 
-def test_step_bytes_match_survey_estimate(lib):
-    # about 12.66 GB per 32-layer step at 128K, batch 8, alpha 0.6, t = 32 (bf16)
+def test_step_bytes_match_the_byte_model_by_hand(lib):
+    # the per-unit byte model worked by hand: about 12.66 GB per 32-layer step at 128K,
+    # batch 8, alpha 0.6, t = 32 (bf16)
     cfg = lib.make_config(LLAMA_128K)
     m = lib.model(cfg, 0.6, 32, 8000.0, 400.0)
     per_step = 32 * (m["hbm_bytes_per_step"])
