@@ -9,12 +9,13 @@
 // key and that mean (Algorithm 1: CosineSimilarity, Min).
 //
 // A tile is 16 chunks = 128 token rows of one (batch, KV head) unit.
-//  * bf16: a tcgen05 tile.  The producer lane loads the unit's B slice
-//    (stored transposed, [d][r], K-major) and the 16 chunks' A rows (8 rows
-//    each, from anywhere in A) with 2-D TMA copies in 64-column (128-byte,
-//    swizzled) blocks; zero fill covers columns past r.  One elected thread
-//    issues M=128, N=128, K=16 bf16 MMAs with an fp32 accumulator in tensor
-//    memory; the four warps read their 32 rows back with tcgen05.ld.
+//  * bf16: a tcgen05 tile.  Once the tile is known to have work, one thread
+//    issues the unit's B slice (stored transposed, [d][r], K-major) while the
+//    chunk list is read, then sixteen threads issue the chunks' A rows (8 rows
+//    each, from anywhere in A); all are 2-D TMA copies in 64-column (128-byte,
+//    swizzled) blocks, and zero fill covers columns past r.  One elected
+//    thread issues M=128, N=128, K=16 bf16 MMAs with an fp32 accumulator in
+//    tensor memory; the four warps read their 32 rows back with tcgen05.ld.
 //  * fp32: CUDA-core FMAs, one thread per row, B broadcast from shared memory
 //    (tf32 tensor cores would not meet fp32 accuracy).
 // Epilogue (both): the fp32 tile is staged in shared memory (the operand
@@ -24,6 +25,10 @@
 // table read and key store is contiguous across the warp; then either the
 // bf16/fp32 key rows go to their destination slot, or the statistics are
 // formed in fp32.
+//
+// Also here: pre-filling from exact keys (the rows come from the caller's keys
+// instead of A.B) and ShadowKV+'s projection of a generated token's key onto
+// the rank-r basis.
 #include <math_constants.h>
 
 #include "skv_common.cuh"
