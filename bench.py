@@ -29,11 +29,15 @@ sys.path.insert(0, ROOT)
 
 from workload import ALL, LLAMA_128K, Workload  # noqa: E402
 
-# DRAM traffic of one k_score_tc launch from an ncu capture (dram__bytes_read.sum +
-# dram__bytes_write.sum = 133.89 + 4.35 MB over 32 units at 128K, bf16), valid only while
-# the scorer source is the one that was profiled; per unit, scaled to a launch by its units.
-SCORE_TRAFFIC = {"source_sha256": "6b81a89c450e7c0b18c603f24db0192aae24ae37004b7445e69bd0cdc73c951f",
-                 "seq_len": 131072, "dtype": "bf16", "bytes_per_unit": (133885696 + 4347136) / 32}
+# DRAM traffic of one scorer launch from ncu captures (dram__bytes_read.sum +
+# dram__bytes_write.sum), valid only while the scorer source is the one that was profiled;
+# per unit, scaled to a launch by its units.  bf16: k_score_tc at 128K b4 (32 units),
+# 133.89 + 4.35 MB; fp8: k_score_f8 at 128K b8 (64 units), 133.94 + 5.40 MB.
+SCORE_TRAFFIC_SHA256 = "6b81a89c450e7c0b18c603f24db0192aae24ae37004b7445e69bd0cdc73c951f"
+SCORE_TRAFFIC = {
+    "bf16": {"seq_len": 131072, "bytes_per_unit": (133885696 + 4347136) / 32},
+    "fp8": {"seq_len": 131072, "bytes_per_unit": (133939712 + 5395456) / 64},
+}
 
 
 METRIC = "sparse decode-attention tokens/s and HBM GB/s (% of 8 TB/s) at 128K, 1×GB300"
@@ -117,8 +121,8 @@ def score_traffic_per_launch(w: Workload):
     src = os.path.join(ROOT, "sparse_kv_cache_gb300", "csrc", "k_score.cu")
     with open(src, "rb") as f:
         digest = hashlib.sha256(f.read()).hexdigest()
-    t = SCORE_TRAFFIC
-    if digest != t["source_sha256"] or w.seq_len != t["seq_len"] or w.dtype != t["dtype"]:
+    t = SCORE_TRAFFIC.get(w.dtype)
+    if digest != SCORE_TRAFFIC_SHA256 or t is None or w.seq_len != t["seq_len"]:
         return None
     return t["bytes_per_unit"] * w.units
 

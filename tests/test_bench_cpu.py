@@ -45,12 +45,14 @@ def test_variant_names_say_what_changed():
 
 def test_scorer_traffic_only_for_the_measured_source(monkeypatch):
     real = bench.score_traffic_per_launch(LLAMA_128K)
-    monkeypatch.setattr(bench, "SCORE_TRAFFIC", dict(bench.SCORE_TRAFFIC, source_sha256="0" * 64))
+    monkeypatch.setattr(bench, "SCORE_TRAFFIC_SHA256", "0" * 64)
     assert bench.score_traffic_per_launch(LLAMA_128K) is None          # another source
     monkeypatch.undo()
     if real is None:
         pytest.skip("the scorer source differs from the profiled one")
-    assert real == pytest.approx(bench.SCORE_TRAFFIC["bytes_per_unit"] * LLAMA_128K.units)
+    assert real == pytest.approx(bench.SCORE_TRAFFIC["bf16"]["bytes_per_unit"] * LLAMA_128K.units)
     assert bench.score_traffic_per_launch(LLAMA_128K.with_(batch=4)) == pytest.approx(real / 2)   # per unit
-    assert bench.score_traffic_per_launch(LLAMA_128K.with_(dtype="fp8")) is None                 # other dtype
+    f8 = bench.score_traffic_per_launch(LLAMA_128K.with_(dtype="fp8"))                           # its own capture
+    assert f8 == pytest.approx(bench.SCORE_TRAFFIC["fp8"]["bytes_per_unit"] * LLAMA_128K.units)
+    assert bench.score_traffic_per_launch(LLAMA_128K.with_(dtype="f32")) is None                 # not captured
     assert bench.score_traffic_per_launch(LLAMA_128K.with_(seq_len=65536)) is None               # other length
