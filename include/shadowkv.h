@@ -64,12 +64,14 @@ typedef enum { SKV_V_HBM = 0, SKV_V_HOST = 1 } skv_vplace;
  *   set as it is.
  * SKV_NEWKEYS_LOWRANK: ShadowKV+ (summary page, "The ShadowKV+ extension for
  *   generated tokens"; digest section A7 on newly generated tokens).  k_new is
- *   the PRE-RoPE key; the library keeps only its rank-r state a = k'.Psi,
- *   where k' [H*d] is the token's key over the H heads of its batch element and
- *   Psi = B^T (B_b read as [r][H*d]), stored like A.  At every step each
- *   generated token i's key is rebuilt as RoPE_{S+i}(a_i . B[b][h]), the same
- *   reconstruction as for context keys.  For a true projection B_b's rows
- *   should be orthonormal (B = Psi^T from the SVD); the library does not check.
+ *   the PRE-RoPE key; the library keeps its rank-r state a = k'.Psi, where k'
+ *   [H*d] is the token's key over the H heads of its batch element and
+ *   Psi = B^T (B_b read as [r][H*d]), stored like A, and attends with the key
+ *   rebuilt from the stored state, RoPE_{S+t}(a . B[b][h]) -- the same
+ *   reconstruction as for context keys, made once when the token arrives and
+ *   kept in the local rows as rebuilt context keys are kept in cache slots.
+ *   For a true projection B_b's rows should be orthonormal (B = Psi^T from the
+ *   SVD); the library does not check.
  */
 typedef enum { SKV_NEWKEYS_EXACT = 0, SKV_NEWKEYS_LOWRANK = 1 } skv_newkeys;
 
@@ -159,8 +161,8 @@ int shadowkv_prefill_index_keys(const skv_config* cfg, const void* A, const void
  *
  *   q      dev [b][H*G][d]  post-RoPE queries at position S + t
  *   k_new  dev [b][H][d]    post-RoPE key of the new token (SKV_NEWKEYS_LOWRANK:
- *                           its pre-RoPE key; step 1 then stores a = k'.Psi and
- *                           step 4 also rebuilds every generated token's key)
+ *                           its pre-RoPE key; step 4 then stores a = k'.Psi and
+ *                           the new token's key rebuilt from it)
  *   v_new  dev [b][H][d]
  *   out    dev [b][H*G][d]  written
  *   sel_out dev int32 [b][H][K] or NULL: I as original chunk ids, ascending

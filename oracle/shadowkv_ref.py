@@ -30,8 +30,8 @@ Readings where the pages are silent (each is also listed in the design notes):
 * The softmax of the selection runs over the n_c selectable chunks only.
 * The query and the new key arrive post-RoPE at position S+t.
 * ShadowKV+ (generated keys at rank r): the new key arrives pre-RoPE, over all
-  H heads of its batch element, and is kept only as k' Psi with Psi = B^T; at
-  every step each generated token's key is rebuilt as RoPE(a.B_h) at S+t.
+  H heads of its batch element, and is kept as k' Psi with Psi = B^T; attention
+  uses each generated token's key rebuilt from that state, RoPE(a.B_h) at S+t.
 
 Parity pins: see ``tests/test_oracle_pins.py`` and ``tests/test_golden.py``.
 The selection scores' near-tie band is not pinned by the pages (no page prints

@@ -82,13 +82,12 @@ struct skv_layer {
     int newkeys = SKV_NEWKEYS_EXACT;
     int Tpad = 0;                         // max_new_tokens rounded up to whole chunks
     void* Anew = nullptr;                 // ShadowKV+: rank-r states of generated tokens, [b][Tpad][r]
-    CUtensorMap tmAnew{};
     uint8_t* qt = nullptr;                // e5m2 scorer: the query's three terms, [U][3G][d]
     float* qinv = nullptr;                // e5m2 scorer: 2^-s per head, [U][G]
     int64_t t = 0, t_reset = 0;
     cudaStream_t last_main = nullptr, last_side = nullptr;
     bool stepped = false;
-    cudaEvent_t ev_sel = nullptr, ev_fetch = nullptr;
+    cudaEvent_t ev_sel = nullptr, ev_fetch = nullptr, ev_start = nullptr;
     bool profiling = false;
     std::vector<std::array<cudaEvent_t, 7>> prof_pending, prof_free;
     double phase_ms[SKV_NPHASE] = {0};
@@ -122,6 +121,7 @@ void free_all(skv_layer* h) {
     h->allocs.clear();
     if (h->ev_sel) cudaEventDestroy(h->ev_sel);
     if (h->ev_fetch) cudaEventDestroy(h->ev_fetch);
+    if (h->ev_start) cudaEventDestroy(h->ev_start);
     for (auto& a : h->prof_pending)
         for (auto e : a) cudaEventDestroy(e);
     for (auto& a : h->prof_free)
@@ -206,11 +206,9 @@ void step_bytes(const skv_config& c, int64_t t, double misses, double* hbm, doub
     h += misses * C * (es * r + es * d + esv * d);   // A rows read, K and V rows written into slots
     h += (misses > 0 ? U : 0.0) * es * r * d;        // B slices
     if (c.new_keys == SKV_NEWKEYS_LOWRANK) {
-        // ShadowKV+: the append writes no key (-U d), the projection reads k' (+U d) and B (U r d)
-        // and writes a (b r); the rebuild of the generated tokens, whole chunks at a time, reads
-        // their rank-r rows (b rows r) and B again (U r d) and writes their keys (U rows d)
-        const double rows = std::ceil((t + 1) / C) * C;
-        h += es * (2.0 * U * r * d + c.batch * r * (1.0 + rows) + U * rows * d);
+        // ShadowKV+: the projection reads k' instead of the append reading the key (no change)
+        // and B (U r d) and writes a (b r); the new key reads a (U r) and B_h again (U r d)
+        h += es * (2.0 * U * r * d + c.batch * r + U * r);
     }
     double l = misses * C * d * esv;                 // value rows over the host link
     if (c.v_place == SKV_V_HBM) { h += l; l = 0.0; }
@@ -340,9 +338,9 @@ int shadowkv_prefill_index_keys(const skv_config* cfg, const void* A, const void
     h->nkb = (h->r + 63) / 64;
     h->newkeys = c.new_keys;
     h->Tpad = (h->Tmax + kC - 1) / kC * kC;
-    // ShadowKV+ rebuilds generated keys a whole chunk (8 rows) at a time
-    h->loc_cap = h->W + (h->newkeys == SKV_NEWKEYS_LOWRANK ? h->Tpad : h->Tmax);
-    h->nhi = static_cast<int>((c.seq_len + (h->newkeys == SKV_NEWKEYS_LOWRANK ? h->Tpad : 0) + 255) / 256);
+    h->loc_cap = h->W + h->Tmax;
+    // ShadowKV+ rotates generated keys at positions S .. S + max_new_tokens - 1 itself
+    h->nhi = static_cast<int>((c.seq_len + (h->newkeys == SKV_NEWKEYS_LOWRANK ? h->Tmax : 0) + 255) / 256);
     h->A = A;
     h->B = B;
     h->V = V;
@@ -434,7 +432,8 @@ int shadowkv_prefill_index_keys(const skv_config* cfg, const void* A, const void
     if ((rc = alloc(h, &Lfull, static_cast<size_t>(U) * h->ncand * kD * 4))) return fail(rc);
     if (h->tc && (rc = alloc(h, &h->Bt, static_cast<size_t>(U) * h->r * kD * 2))) return fail(rc);
     if (cudaEventCreateWithFlags(&h->ev_sel, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&h->ev_fetch, cudaEventDisableTiming) != cudaSuccess)
+        cudaEventCreateWithFlags(&h->ev_fetch, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_start, cudaEventDisableTiming) != cudaSuccess)
         return fail(SKV_ERR_CUDA);
 
     // RoPE tables in double precision: angle(pos) = (pos & 255)*theta + (pos >> 8)*256*theta
@@ -468,8 +467,7 @@ int shadowkv_prefill_index_keys(const skv_config* cfg, const void* A, const void
             (rc = make_map(&h->tmB, h->Bt, h->r, static_cast<uint64_t>(U) * kD, 128)) ||
             (rc = h->dtype == SKV_FP8 ? make_map_u8(&h->tmL, h->L, kD, static_cast<uint64_t>(U) * h->n_c, kScTile)
                                       : make_map(&h->tmL, h->L, kD, static_cast<uint64_t>(U) * h->n_c, kScTile)) ||
-            (rc = make_map(&h->tmKall, h->Kall, kD, static_cast<uint64_t>(U) * h->R, 128)) ||
-            (h->Anew && (rc = make_map(&h->tmAnew, h->Anew, h->r, static_cast<uint64_t>(c.batch) * h->Tpad, 8))))
+            (rc = make_map(&h->tmKall, h->Kall, kD, static_cast<uint64_t>(U) * h->R, 128)))
             return fail(rc);
     }
 
@@ -568,6 +566,23 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
         }
         cudaEventRecord(ev[0], sm);
     }
+    if (h->newkeys == SKV_NEWKEYS_LOWRANK) {
+        // ShadowKV+: keep the new token as a = k'.Psi and write its key RoPE_{S+t}(a . B_h) into
+        // local row W + t.  A generated token's key depends only on its fixed rank-r state, so
+        // the rows of earlier generated tokens stay valid: the local rows cache the rebuilt
+        // keys as the cache slots do for context chunks.  This needs only k_new, so it runs on
+        // the side stream beside scoring and selection; attention waits for the side stream.
+        if (ss != sm) {
+            cudaEventRecord(h->ev_start, sm);
+            cudaStreamWaitEvent(ss, h->ev_start, 0);
+        }
+        PlusParams pp{};
+        pp.k_new = k_new; pp.B = h->B; pp.a_new = h->Anew; pp.k_loc = h->Kloc;
+        pp.rope_lo = h->rope_lo; pp.rope_hi = h->rope_hi;
+        pp.H = h->H; pp.r = h->r; pp.t = t;
+        pp.a_rows = h->Tpad; pp.pos = h->S + t; pp.loc_pitch = h->R; pp.loc_row = h->W + t;
+        if (launch_plus_append(h->dtype == SKV_F32 ? 0 : 1, pp, U / h->H, ss)) return SKV_ERR_CUDA;
+    }
     // a2: landmark scoring
     ScoreParams sp{};
     sp.L = h->L; sp.q = q; sp.logits = h->logits; sp.part = h->score_part; sp.n_c = h->n_c;
@@ -614,23 +629,6 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     const int gx = (K + kTileChunks - 1) / kTileChunks;
     const int rc = h->tc ? launch_rebuild_tc(&h->tmA, &h->tmB, rp, gx, sm) : launch_rebuild_f32(rp, gx, sm);
     if (rc) return SKV_ERR_CUDA;
-    if (h->newkeys == SKV_NEWKEYS_LOWRANK) {
-        // ShadowKV+: keep the new token as a = k'.Psi, then rebuild every generated token's key
-        // RoPE_{S+i}(a_i . B_h) into local rows W + i, whole chunks at a time
-        const int batch = U / h->H;
-        if (launch_project(h->dtype == SKV_F32 ? 0 : 1, k_new, h->B, h->Anew, batch, h->H, h->r, h->Tpad, t, sm))
-            return SKV_ERR_CUDA;
-        const int nch = t / kC + 1;
-        RebuildParams rn = rp;
-        rn.S = h->Tpad; rn.pos_base = h->S; rn.nchunk = h->Tpad / kC;
-        rn.list = nullptr; rn.list_us = 0; rn.list_base = 0; rn.list_cap = h->Tpad / kC;
-        rn.cnt = nullptr; rn.count_const = nch; rn.dst_idx = nullptr; rn.dst_cap = h->Tpad / kC;
-        rn.dst = static_cast<uint8_t*>(h->Kloc) + static_cast<size_t>(h->W) * kD * h->es;
-        rn.A = h->Anew;
-        const int gxn = (nch + kTileChunks - 1) / kTileChunks;
-        if (h->tc ? launch_rebuild_tc(&h->tmAnew, &h->tmB, rn, gxn, sm) : launch_rebuild_f32(rn, gxn, sm))
-            return SKV_ERR_CUDA;
-    }
     if (h->profiling) cudaEventRecord(ev[3], sm);
     if (ss != sm) cudaStreamWaitEvent(sm, h->ev_fetch, 0);
     // a7: attention over outliers + cache + local, split-K with an in-kernel merge
@@ -647,7 +645,7 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     const int na = h->tc ? launch_attn_tc(&h->tmKall, ap, h->sm_count, sm) : (launch_attn(h->dtype, ap, sm) ? -1 : 1);
     if (na < 0) return SKV_ERR_CUDA;
     // score, select, fetch, rebuild, attention (+ its merge); the e5m2 query split; ShadowKV+'s
-    // projection and generated-key rebuild
+    // projection and new key
     h->launches += 4 + na + (h->dtype == SKV_FP8 ? 1 : 0) + (h->newkeys == SKV_NEWKEYS_LOWRANK ? 2 : 0);
     if (h->profiling) {
         cudaEventRecord(ev[4], sm);

@@ -71,7 +71,7 @@ struct RopeRegs {
 __device__ __forceinline__ void rope_fetch(const RebuildParams& p, const TileInfo& t, RopeRegs& r) {
     const int lane = threadIdx.x & 31;
     if (t.chunk < 0) return;
-    const int64_t pos0 = p.pos_base + static_cast<int64_t>(t.chunk) * kC;
+    const int pos0 = t.chunk * kC;
     r.hi = reinterpret_cast<const float4*>(p.rope_hi + (pos0 >> 8) * (kD / 2))[lane];
 #pragma unroll
     for (int i = 0; i < kC; ++i) r.lo[i] = reinterpret_cast<const float4*>(p.rope_lo + ((pos0 + i) & 255) * (kD / 2))[lane];
@@ -446,7 +446,7 @@ int launch_keys_exact(const RebuildParams& p, int grid_x, bool out_bf16, cudaStr
     return e == cudaSuccess ? 0 : -1;
 }
 
-// ------------------------------------------------------------------ ShadowKV+ projection
+// ------------------------------------------------------------------ ShadowKV+ append
 // The rank-r state of a generated token (summary page, "The ShadowKV+ extension
 // for generated tokens"): a[j] = sum over heads h and dims i of k'[h][i] * B[h][j][i],
 // i.e. k' (the token's pre-RoPE key over the H heads) times Psi = B^T.  Block
@@ -492,6 +492,59 @@ int launch_project(int dtype, const void* k_new, const void* B, void* a_new, int
         k_project<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(k_new),
                                                       static_cast<const __nv_bfloat16*>(B),
                                                       static_cast<__nv_bfloat16*>(a_new), H, r, a_rows, t);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+// Then head h's key of the new token from the stored state: x = a . B_h, thread (g, c) summing
+// rows j = g, g + 8, ... of column chunk c (eight dims), the 8 row groups summed in order, and
+// RoPE at position pos with the angle composed from the (pos & 255) and (pos >> 8) tables.
+// Small (128 threads, ~5 KB of shared memory) so that it fits beside the scorer.
+template <typename T>
+__global__ void __launch_bounds__(128) k_plus_key(PlusParams p) {
+    extern __shared__ float sh_plus[];
+    float* a_s = sh_plus;                         // [r]
+    float* xp = a_s + p.r;                        // [8][d]
+    const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+    const T* a = static_cast<const T*>(p.a_new) + (static_cast<int64_t>(b) * p.a_rows + p.t) * p.r;
+    for (int j = tid; j < p.r; j += 128) a_s[j] = to_f(a[j]);
+    __syncthreads();
+    const int c = tid & 15, g = tid >> 4;
+    const T* bh = static_cast<const T*>(p.B) + (static_cast<int64_t>(b) * p.H + h) * p.r * kD + 8 * c;
+    float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+    for (int j = g; j < p.r; j += 8) {
+        float v[8];
+        load8(bh + static_cast<int64_t>(j) * kD, v);
+        const float aj = a_s[j];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = fmaf(aj, v[e], x[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) xp[g * kD + 8 * c + e] = x[e];
+    __syncthreads();
+    if (tid < kD / 2) {
+        float y1 = 0.f, y2 = 0.f;
+        for (int gg = 0; gg < 8; ++gg) {
+            y1 += xp[gg * kD + tid];
+            y2 += xp[gg * kD + tid + kD / 2];
+        }
+        const int64_t pos = p.pos;
+        const float2 lo = p.rope_lo[(pos & 255) * (kD / 2) + tid];
+        const float2 hi = p.rope_hi[(pos >> 8) * (kD / 2) + tid];
+        const float cs = hi.x * lo.x - hi.y * lo.y, sn = hi.y * lo.x + hi.x * lo.y;
+        T* dst = static_cast<T*>(p.k_loc) + ((static_cast<int64_t>(b) * p.H + h) * p.loc_pitch + p.loc_row) * kD;
+        dst[tid] = from_f<T>(y1 * cs - y2 * sn);
+        dst[tid + kD / 2] = from_f<T>(y1 * sn + y2 * cs);
+    }
+}
+
+int launch_plus_append(int dtype, const PlusParams& p, int batch, cudaStream_t s) {
+    if (p.r > 256 || p.H < 1) return -1;
+    if (launch_project(dtype, p.k_new, p.B, p.a_new, batch, p.H, p.r, p.a_rows, p.t, s)) return -1;
+    const dim3 grid(batch, p.H);
+    const size_t smem = static_cast<size_t>(p.r + 8 * kD) * sizeof(float);
+    if (dtype == 0) k_plus_key<float><<<grid, 128, smem, s>>>(p);
+    else k_plus_key<__nv_bfloat16><<<grid, 128, smem, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

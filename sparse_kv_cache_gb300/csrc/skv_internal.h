@@ -87,8 +87,7 @@ int launch_select_outliers(const SelectParams& p, cudaStream_t s);
 struct RebuildParams {
     int mode;                 // 0: store RoPE'd keys, 1: landmark + min-cos statistics
     int U, H, r, nkb;
-    int64_t S;                // rows of A per batch element (chunk c of batch b: rows b*S + 8c ...)
-    int64_t pos_base;         // RoPE position of chunk c's first row: pos_base + 8c
+    int64_t S;                // context length: rows of A per batch element
     int nchunk;               // S / C, bound on chunk ids
     const int32_t* list;      // [U][list_us] chunk ids, or NULL: chunk = list_base + index
     int64_t list_us; int list_base; int list_cap;
@@ -113,9 +112,16 @@ int launch_rebuild_f32(const RebuildParams& p, int grid_x, cudaStream_t s);
 // the same outputs from exact pre-RoPE keys p.Kx instead of A.B (keys stored as bf16 when out_bf16)
 int launch_keys_exact(const RebuildParams& p, int grid_x, bool out_bf16, cudaStream_t s);
 int launch_transpose_B(const void* B, void* Bt, int U, int r, cudaStream_t s);
-// ShadowKV+: a[b] = k'[b] . B_b^T (k' [b][H][d], B [b][H][r][d]) into row t of a_new [b][a_rows][r]
-int launch_project(int dtype, const void* k_new, const void* B, void* a_new, int batch, int H, int r,
-                   int64_t a_rows, int t, cudaStream_t s);
+// ShadowKV+ append: a[b] = k'[b] . B_b^T (k' [b][H][d], B [b][H][r][d]) into row t of
+// a_new [b][a_rows][r], and every head's key RoPE_pos(a . B_h) into local row loc_row of its
+// unit (rows of loc_pitch per unit)
+struct PlusParams {
+    const void* k_new; const void* B; void* a_new; void* k_loc;
+    const float2* rope_lo; const float2* rope_hi;
+    int H, r, t;
+    int64_t a_rows, pos, loc_pitch, loc_row;
+};
+int launch_plus_append(int dtype, const PlusParams& p, int batch, cudaStream_t s);
 
 struct GatherParams {
     const void* src; int64_t src_us;   // rows of unit u start at src + u*src_us (elements)
