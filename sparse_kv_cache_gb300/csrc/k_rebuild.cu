@@ -208,6 +208,8 @@ __global__ void __launch_bounds__(128, 1) k_rebuild_tc(const __grid_constant__ C
     // units along x, tiles along y: the first tiles of every unit are dispatched before any
     // unit's later (often empty) ones
     const int u = blockIdx.x, tile = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
+    // launched as a programmatic dependent of the selection: the list is its output
+    pdl_wait();
     // the list entries are read in the same round trip as the count (in bounds up to list_cap)
     int ch_raw = 0, dst_raw = 0;
     const int first_idx = tile * kTileChunks;
@@ -571,8 +573,11 @@ int launch_rebuild_tc(const CUtensorMap* tmA, const CUtensorMap* tmB, const Rebu
     const size_t smem = tc_smem(p);
     auto fn = k_rebuild_tc<__nv_bfloat16>;
     cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    fn<<<dim3(p.U, grid_x), 128, smem, s>>>(*tmA, *tmB, p);
-    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+    if (launch_pdl(fn, dim3(p.U, grid_x), dim3(128), smem, s, *tmA, *tmB, p) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    return 0;
 }
 
 int launch_rebuild_f32(const RebuildParams& p, int grid_x, cudaStream_t s) {
