@@ -597,6 +597,7 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     sel.n = h->n_c; sel.k = K; sel.U = U; sel.H = h->H; sel.G = G;
     sel.logits = h->logits; sel.part = h->score_part; sel.nru = h->score_nru; sel.nparts = h->score_nparts;
     sel.sched = h->sched; sel.vbuf = h->vbuf; sel.smem_cap = h->sel_smem_cap; sel.ids = h->ids;
+    sel.nsm = h->sm_count;
     sel.sel_out_user = sel_out; sel.t = t;
     sel.prev_ids = h->sel_ids[t & 1]; sel.prev_slot = h->sel_slot[t & 1];
     sel.cur_ids = h->sel_ids[(t + 1) & 1]; sel.cur_slot = h->sel_slot[(t + 1) & 1];

@@ -20,6 +20,8 @@
 // order by a two-pass warp-segmented compaction.
 #include <math_constants.h>
 
+#include <algorithm>
+
 #include "skv_common.cuh"
 #include "skv_internal.h"
 
@@ -41,6 +43,8 @@ struct SelShared {
     float lse[8];
     float vmin, vmax, T;
     int jlast, bstar, above, total;
+    float cl_lo, cl_hi;   // cluster form: this CTA's score range and counts, read by the others
+    int cl_cnt;
 };
 
 __device__ __forceinline__ uint32_t ord_key(float x) {
@@ -208,6 +212,185 @@ __device__ void topk_threshold(const float* vals, int n, int k, SelShared& sh, i
     __syncthreads();
 }
 
+// The same threshold over a unit's scores split into C contiguous slices, one per CTA of a
+// cluster (this CTA: rank `rank`, scores vals[0..nl) at global positions j0 + ...).  Every
+// decision is taken on cluster-wide sums, so every CTA reaches the same T and jlast (global
+// positions) as the one-CTA form: the score range, the histogram and each radix digit's
+// counts are summed over the cluster; boundary candidates are gathered in the leader (rank 0),
+// which ranks them; the jlast of a crowded bin is found by the CTA holding it.  All branches
+// are uniform across the cluster, so every CTA passes every cluster barrier.
+__device__ void topk_threshold_cl(const float* vals, int nl, int j0, int k, SelShared& sh, int* err, float lo, float hi,
+                                  int C, int rank) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    lo = warp_min(lo);
+    hi = warp_max(hi);
+    if (lane == 0) { sh.red_f[warp] = lo; sh.red_f2[warp] = hi; }
+    for (int b = tid; b < kBins; b += kSelThreads) sh.hist[b] = 0;
+    if (tid == 0) sh.ncand = 0;
+    __syncthreads();
+    if (warp == 0) {
+        lo = warp_min(sh.red_f[lane]);
+        hi = warp_max(sh.red_f2[lane]);
+        if (lane == 0) { sh.cl_lo = lo; sh.cl_hi = hi; }
+    }
+    cluster_sync_all();   // every CTA's range is published; every candidate counter is zero
+    if (tid == 0) {
+        float L = CUDART_INF_F, Hh = -CUDART_INF_F;
+        for (int r = 0; r < C; ++r) {
+            L = fminf(L, ld_cluster_f32(cluster_addr(&sh.cl_lo, r)));
+            Hh = fmaxf(Hh, ld_cluster_f32(cluster_addr(&sh.cl_hi, r)));
+        }
+        sh.vmin = L;
+        sh.vmax = Hh;
+    }
+    __syncthreads();
+    const float vmin = sh.vmin, vmax = sh.vmax;
+    if (!(vmax > vmin)) {
+        // all scores equal (or not finite): the k lowest positions
+        if (tid == 0) {
+            sh.T = vmax;
+            sh.jlast = k - 1;
+            if (rank == 0 && (!(vmax == vmax) || isinf(vmax))) set_err(err, DEV_ERR_NUMERIC, 301);
+        }
+        cluster_sync_all();   // nobody reads another CTA's range after this
+        return;
+    }
+    float invw = static_cast<float>(kBins) / (vmax - vmin);
+    if (!isfinite(invw)) invw = 0.f;
+#pragma unroll 4
+    for (int j = tid; j < nl; j += kSelThreads) atomicAdd(&sh.hist[bin_of(vals[j], vmin, invw)], 1);
+    cluster_sync_all();   // every CTA's histogram is complete
+    {
+        const int b0 = kBins - 1 - 2 * tid, b1 = b0 - 1;
+        int h0 = 0, h1 = 0;
+        for (int r = 0; r < C; ++r) {
+            h0 += ld_cluster_s32(cluster_addr(&sh.hist[b0], r));
+            h1 += ld_cluster_s32(cluster_addr(&sh.hist[b1], r));
+        }
+        const int above = block_exscan(h0 + h1, sh, nullptr);
+        if (above < k && k <= above + h0 + h1) {
+            const bool first = above + h0 >= k;
+            sh.bstar = first ? b0 : b1;
+            sh.above = first ? above : above + h0;
+            sh.total = first ? h0 : h1;   // the boundary bin's count over the cluster
+        }
+    }
+    __syncthreads();
+    const int bstar = sh.bstar, need = k - sh.above, cnt = sh.total;
+    cluster_sync_all();   // every CTA has read the histograms
+    if (cnt <= kCand) {
+        // the boundary bin's members, gathered in the leader, ranked there
+        const uint32_t lead_n = cluster_addr(&sh.ncand, 0);
+        for (int j = tid; j < nl; j += kSelThreads) {
+            const float x = vals[j];
+            if (bin_of(x, vmin, invw) == bstar) {
+                const int c = atom_cluster_add(lead_n, 1);
+                if (c < kCand) {
+                    st_cluster_f32(cluster_addr(&sh.cand_v[c], 0), x);
+                    st_cluster_s32(cluster_addr(&sh.cand_j[c], 0), j0 + j);
+                }
+            }
+        }
+        cluster_sync_all();
+        if (rank == 0) {
+            const int nc = min(sh.ncand, kCand);
+            if (tid < nc) {
+                const float x = sh.cand_v[tid];
+                const int jx = sh.cand_j[tid];
+                int rnk = 0;
+                for (int m = 0; m < nc; ++m) {
+                    const float y = sh.cand_v[m];
+                    rnk += (y > x) || (y == x && sh.cand_j[m] < jx);
+                }
+                if (rnk == need - 1) { sh.T = x; sh.jlast = jx; }
+            }
+        }
+        cluster_sync_all();   // the leader's T and jlast are set
+        if (tid == 0 && rank != 0) {
+            sh.T = ld_cluster_f32(cluster_addr(&sh.T, 0));
+            sh.jlast = ld_cluster_s32(cluster_addr(&sh.jlast, 0));
+        }
+        cluster_sync_all();   // nobody reads the leader after this
+        return;
+    }
+    // crowded boundary bin: exact radix select on the order-preserving keys, digit counts summed
+    uint32_t prefix = 0, mask = 0;
+    int rem = need;
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        for (int b = tid; b < 256; b += kSelThreads) sh.hist[b] = 0;
+        __syncthreads();
+        for (int j = tid; j < nl; j += kSelThreads) {
+            const float x = vals[j];
+            if (bin_of(x, vmin, invw) != bstar) continue;
+            const uint32_t key = ord_key(x);
+            if ((key & mask) == prefix) atomicAdd(&sh.hist[(key >> shift) & 255], 1);
+        }
+        cluster_sync_all();   // every CTA's digit counts are complete
+        if (tid == 0) {
+            int c = 0, d = 255;
+            for (; d > 0; --d) {
+                int hd = 0;
+                for (int r = 0; r < C; ++r) hd += ld_cluster_s32(cluster_addr(&sh.hist[d], r));
+                if (c + hd >= rem) break;
+                c += hd;
+            }
+            sh.above = c;
+            sh.bstar = d;
+        }
+        cluster_sync_all();   // every CTA has read the counts before the next pass clears them
+        rem -= sh.above;
+        prefix |= static_cast<uint32_t>(sh.bstar) << shift;
+        mask |= 0xFFu << shift;
+    }
+    const float T = key_to_float(prefix);
+    // jlast: the rem-th score equal to T in position order; slices are in position order
+    int c = 0;
+    for (int j = tid; j < nl; j += kSelThreads) c += vals[j] == T;
+    c = warp_sum_i(c);
+    if (lane == 0) sh.red_i[warp] = c;
+    __syncthreads();
+    if (tid == 0) {
+        int t = 0;
+        for (int w = 0; w < kWarps; ++w) t += sh.red_i[w];
+        sh.cl_cnt = t;
+    }
+    cluster_sync_all();   // every CTA's count of ties is published
+    if (tid == 0) {
+        int base = 0;
+        for (int r = 0; r < rank; ++r) base += ld_cluster_s32(cluster_addr(&sh.cl_cnt, r));
+        sh.above = base;
+    }
+    __syncthreads();
+    const int base = sh.above;
+    if (rem - 1 >= base && rem - 1 < base + sh.cl_cnt) {
+        // this CTA holds it: warp-segmented scan of the slice in position order
+        const int seg = ((nl + kWarps - 1) / kWarps + 31) & ~31;
+        const int a = warp * seg, e = min(nl, a + seg);
+        int cw = 0;
+        for (int j = a + lane; j < a + seg; j += 32) {
+            const bool eq = j < e && vals[j] == T;
+            cw += __popc(__ballot_sync(0xffffffffu, eq));
+        }
+        int tot2 = 0;
+        const int wbase = block_exscan(lane == 0 ? cw : 0, sh, &tot2);
+        int run = base + __shfl_sync(0xffffffffu, wbase, 0);
+        for (int j = a + lane; j < a + seg; j += 32) {
+            const bool eq = j < e && vals[j] == T;
+            const unsigned bal = __ballot_sync(0xffffffffu, eq);
+            const int r = run + __popc(bal & ((1u << lane) - 1u));
+            if (eq && r == rem - 1) st_cluster_s32(cluster_addr(&sh.jlast, 0), j0 + j);
+            run += __popc(bal);
+        }
+    }
+    cluster_sync_all();   // the leader's jlast is set
+    if (tid == 0) {
+        sh.T = T;
+        if (rank != 0) sh.jlast = ld_cluster_s32(cluster_addr(&sh.jlast, 0));
+    }
+    cluster_sync_all();   // nobody reads the leader after this
+}
+
 // Writes the selected indices (ascending) via out_fn(pos, j); returns the count.
 // Element j lives in row r = j / kSelThreads at thread j % kSelThreads, so a row
 // is in index order across the block.  One read per element: warp w counts its
@@ -279,22 +462,29 @@ __device__ __forceinline__ int lower_bound(const int32_t* a, int n, int x) {
 }
 
 // ----------------------------------------------------------------- decode
-template <int G>
+template <int G, bool CL>
 __global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
     extern __shared__ __align__(16) uint8_t dsm[];
     __shared__ SelShared sh;
-    const int u = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // cluster form (CL): the unit's scores are split into C contiguous slices, one per CTA of a
+    // cluster; the leader (rank 0) appends, gathers the selection and does the index scan
+    const int C = CL ? p.cluster : 1;
+    const int crank = CL ? static_cast<int>(cluster_ctarank()) : 0;
+    const int u = blockIdx.x / C, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n = p.n, K = p.k;
+    const int j0 = static_cast<int>(static_cast<int64_t>(crank) * n / C);
+    const int nl = static_cast<int>(static_cast<int64_t>(crank + 1) * n / C) - j0;
+    const int nlmax = (n + C - 1) / C;
     pdl_wait();      // the scores of this step
     pdl_trigger();
-    float* vals = (n <= p.smem_cap) ? reinterpret_cast<float*>(dsm) : p.vbuf + static_cast<int64_t>(u) * n;
-    const int cap_f = (n <= p.smem_cap) ? ((n + 3) & ~3) : 0;
+    float* vals = (nlmax <= p.smem_cap) ? reinterpret_cast<float*>(dsm) : p.vbuf + static_cast<int64_t>(u) * n + j0;
+    const int cap_f = (nlmax <= p.smem_cap) ? ((nlmax + 3) & ~3) : 0;
     int32_t* sSel = reinterpret_cast<int32_t*>(dsm) + cap_f;
     int32_t* sSlot = sSel + K;
     int32_t* sFree = sSlot + K;
     int32_t* sPid = sFree + K;       // previous step's selection (ascending) ...
     int32_t* sPslot = sPid + K;      // ... and its slots
-    if (warp >= G) {
+    if (crank == 0 && warp >= G) {
         // work with no dependency on the scores, done while warps < G form the log-sum-exp
         const int wt = tid - G * 32, nt = kSelThreads - G * 32;
         if (p.t > 0) {
@@ -367,19 +557,19 @@ __global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
         const float S = warp_sum(m == -CUDART_INF_F ? 0.f : sx * __expf(m - M));
         if (lane == 0) sh.lse[warp] = M + __logf(S);
     }
-    if (u == 0 && tid == 0 && p.sched) *p.sched = 0;   // the scoring kernel of this step is done
+    if (u == 0 && crank == 0 && tid == 0 && p.sched) *p.sched = 0;   // the scoring kernel of this step is done
     __syncthreads();
     // 2. v_j = max_g (z_gj - lse_g)
     float lse[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) lse[g] = sh.lse[g];
-    const float* z = p.logits + static_cast<int64_t>(u) * n * G;
+    const float* z = p.logits + (static_cast<int64_t>(u) * n + j0) * G;   // this CTA's slice
     float lo = CUDART_INF_F, hi = -CUDART_INF_F;
     if constexpr (G == 4) {
         // four independent 16-byte loads in flight per thread
         const float4* z4 = reinterpret_cast<const float4*>(z);
         int j = tid;
-        for (; j + 7 * kSelThreads < n; j += 8 * kSelThreads) {
+        for (; j + 7 * kSelThreads < nl; j += 8 * kSelThreads) {
             float4 a[8];
 #pragma unroll
             for (int r = 0; r < 8; ++r) a[r] = __ldcg(z4 + j + r * kSelThreads);
@@ -391,7 +581,7 @@ __global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
                 hi = fmaxf(hi, v);
             }
         }
-        for (; j < n; j += kSelThreads) {
+        for (; j < nl; j += kSelThreads) {
             const float4 zz = __ldcg(z4 + j);
             const float v = fmaxf(fmaxf(zz.x - lse[0], zz.y - lse[1]), fmaxf(zz.z - lse[2], zz.w - lse[3]));
             vals[j] = v;
@@ -400,7 +590,7 @@ __global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
         }
     } else {
 #pragma unroll 4
-        for (int j = tid; j < n; j += kSelThreads) {
+        for (int j = tid; j < nl; j += kSelThreads) {
             float v = -CUDART_INF_F;
 #pragma unroll
             for (int g = 0; g < G; ++g) v = fmaxf(v, z[static_cast<int64_t>(j) * G + g] - lse[g]);
@@ -410,22 +600,54 @@ __global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
         }
     }
     // 3. exact top-K threshold and ordered compaction into sSel (original chunk ids)
-    topk_threshold(vals, n, K, sh, p.err, lo, hi);
+    if constexpr (CL) topk_threshold_cl(vals, nl, j0, K, sh, p.err, lo, hi, C, crank);
+    else topk_threshold(vals, n, K, sh, p.err, lo, hi);
     const float T = sh.T;
     const int jlast = sh.jlast;
     const int32_t* ids = p.ids + static_cast<int64_t>(u) * n;
-    const int got = compact_selected(vals, n, T, jlast, sh, [&](int pos, int j) {
+    const int got = compact_selected(vals, nl, T, jlast - j0, sh, [&](int pos, int j) {
         if (pos < K) sSel[pos] = j;
     });
-    if (got != K) {
-        // only non-finite scores can break the count; keep downstream indices valid
-        if (tid == 0) set_err(p.err, DEV_ERR_NUMERIC, 312);
-        for (int i = tid; i < K; i += kSelThreads) sSel[i] = i;
+    if constexpr (!CL) {
+        if (got != K) {
+            // only non-finite scores can break the count; keep downstream indices valid
+            if (tid == 0) set_err(p.err, DEV_ERR_NUMERIC, 312);
+            for (int i = tid; i < K; i += kSelThreads) sSel[i] = i;
+            __syncthreads();
+        }
+        // positions -> original chunk ids, every load in flight at once
+        for (int i = tid; i < K; i += kSelThreads) sSel[i] = ids[sSel[i]];
+        __syncthreads();
+    } else {
+        // each CTA translates its slice's picks, then places them after the lower ranks' picks
+        // in the leader's selection
+        const int mine = min(got, K);
+        for (int i = tid; i < mine; i += kSelThreads) sSel[i] = ids[j0 + sSel[i]];
+        if (tid == 0) sh.cl_cnt = got;
+        cluster_sync_all();
+        if (tid == 0) {
+            int base = 0, total = 0;
+            for (int r = 0; r < C; ++r) {
+                const int cr = ld_cluster_s32(cluster_addr(&sh.cl_cnt, r));
+                if (r < crank) base += cr;
+                total += cr;
+            }
+            sh.above = base;
+            sh.total = total;
+        }
+        __syncthreads();
+        const int base = sh.above;
+        if (crank != 0)
+            for (int i = tid; i < mine && base + i < K; i += kSelThreads)
+                st_cluster_s32(cluster_addr(&sSel[base + i], 0), sSel[i]);
+        cluster_sync_all();   // the leader's selection is complete; no CTA reads another after this
+        if (crank != 0) return;
+        if (sh.total != K) {
+            if (tid == 0) set_err(p.err, DEV_ERR_NUMERIC, 312);
+            for (int i = tid; i < K; i += kSelThreads) sSel[i] = ids[i];
+        }
         __syncthreads();
     }
-    // positions -> original chunk ids, every load in flight at once
-    for (int i = tid; i < K; i += kSelThreads) sSel[i] = ids[sSel[i]];
-    __syncthreads();
     // 4. index scan against the previous step's selection.  Entry i's thread looks
     // up sSel[i] among the previous ids (hit: keeps its slot) and the previous
     // entry i among the current ids (gone: its slot is freed), two independent
@@ -523,20 +745,83 @@ __global__ void __launch_bounds__(kSelThreads) k_select_outliers(SelectParams p)
     }
 }
 
+constexpr int kSelMinPerCta = 4096;           // scores per CTA of a cluster, at least
+constexpr int kSelOneCta = 16 * kSelThreads;    // up to this many scores a unit keeps one CTA
+
 int launch_select_decode(int dtype, const SelectParams& p, cudaStream_t s) {
     (void)dtype;
-    const int cap_f = (p.n <= p.smem_cap) ? ((p.n + 3) & ~3) : 0;
-    const size_t smem = static_cast<size_t>(cap_f) * 4 + static_cast<size_t>(p.k) * 4 * 5;
-    void (*fn)(SelectParams) = nullptr;
+    void (*fn)(SelectParams) = nullptr;    // one CTA per unit
+    void (*fnc)(SelectParams) = nullptr;   // a cluster per unit
     switch (p.G) {
-        case 1: fn = k_select_decode<1>; break;
-        case 2: fn = k_select_decode<2>; break;
-        case 4: fn = k_select_decode<4>; break;
-        case 8: fn = k_select_decode<8>; break;
+        case 1: fn = k_select_decode<1, false>; fnc = k_select_decode<1, true>; break;
+        case 2: fn = k_select_decode<2, false>; fnc = k_select_decode<2, true>; break;
+        case 4: fn = k_select_decode<4, false>; fnc = k_select_decode<4, true>; break;
+        case 8: fn = k_select_decode<8, false>; fnc = k_select_decode<8, true>; break;
         default: return -1;
     }
-    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (launch_pdl(fn, dim3(p.U), dim3(kSelThreads), smem, s, p) != cudaSuccess) {
+    // A unit with more than kSelOneCta scores and SMs to spare is split over a cluster of C
+    // CTAs: the largest C <= 16 that leaves every CTA at least kSelMinPerCta scores, fits a
+    // slice in shared memory, and keeps all U clusters resident at once.
+    static int max_clusters[4][17];   // per G, per cluster size; 0 = not queried
+    const int gi = p.G == 1 ? 0 : p.G == 2 ? 1 : p.G == 4 ? 2 : 3;
+    int C = 1;
+    const int cmax = p.n > kSelOneCta ? std::min(16, p.nsm > 0 ? p.nsm / p.U : 1) : 1;
+    if (cmax > 8) cudaFuncSetAttribute(fnc, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    for (int c = cmax; c >= 2 && C == 1; --c) {
+        const int nlmax = (p.n + c - 1) / c;
+        if (p.n / c < kSelMinPerCta || nlmax > p.smem_cap) continue;
+        const size_t sm_c = static_cast<size_t>((nlmax + 3) & ~3) * 4 + static_cast<size_t>(p.k) * 4 * 5;
+        if (max_clusters[gi][c] == 0) {
+            cudaFuncSetAttribute(fnc, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm_c));
+            cudaLaunchConfig_t q = {};
+            q.gridDim = dim3(p.U * c);
+            q.blockDim = dim3(kSelThreads);
+            q.dynamicSmemBytes = sm_c;
+            cudaLaunchAttribute qa[1];
+            qa[0].id = cudaLaunchAttributeClusterDimension;
+            qa[0].val.clusterDim.x = c;
+            qa[0].val.clusterDim.y = 1;
+            qa[0].val.clusterDim.z = 1;
+            q.attrs = qa;
+            q.numAttrs = 1;
+            int nmax = 0;
+            if (cudaOccupancyMaxActiveClusters(&nmax, fnc, &q) != cudaSuccess) {
+                cudaGetLastError();
+                nmax = 0;
+            }
+            max_clusters[gi][c] = nmax > 0 ? nmax : -1;
+        }
+        if (max_clusters[gi][c] >= p.U) C = c;
+    }
+    const int nlmax = (p.n + C - 1) / C;
+    const int cap_f = (nlmax <= p.smem_cap) ? ((nlmax + 3) & ~3) : 0;
+    const size_t smem = static_cast<size_t>(cap_f) * 4 + static_cast<size_t>(p.k) * 4 * 5;
+    if (C == 1) {
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (launch_pdl(fn, dim3(p.U), dim3(kSelThreads), smem, s, p) != cudaSuccess) {
+            cudaGetLastError();
+            return -1;
+        }
+        return 0;
+    }
+    SelectParams pc = p;
+    pc.cluster = C;
+    cudaFuncSetAttribute(fnc, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.U * C);
+    cfg.blockDim = dim3(kSelThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = C;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    if (cudaLaunchKernelEx(&cfg, fnc, pc) != cudaSuccess) {
         cudaGetLastError();
         return -1;
     }

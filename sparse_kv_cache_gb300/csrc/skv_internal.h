@@ -59,6 +59,8 @@ struct SelectParams {
     // decode: scores from logits and score partials
     const float* logits; const float2* part;
     int nru; int nparts;
+    int nsm;              // SMs of the device (decode: picks the cluster form)
+    int cluster;          // set by the launcher: CTAs per unit (1: one CTA per unit)
     int* sched;           // scoring run counter, reset here for the next step
     // outlier mode: score = -src[u][j]
     const float* neg_src;

@@ -38,6 +38,8 @@ class Workload:
     spike_chunks: int = -1     # planted outlier chunks per batch element (-1: 0.3 % of chunks, capped at O)
     spike_scale: float = 6.0
     new_keys: str = "exact"    # "exact": generated keys kept whole; "lowrank": ShadowKV+ (kept at rank r)
+    dense_chunks: int = -1     # >= 0: only the first dense_chunks chunks have nonzero A rows; every
+                               # later chunk has zero keys, so all of them score exactly alike
 
     @property
     def group(self) -> int:

@@ -86,6 +86,8 @@ def make_A(w: Workload, layer: int, device="cpu") -> torch.Tensor:
     e[:, 1:] *= math.sqrt(1.0 - w.ar_rho ** 2)
     A = ar1_scan(e, w.ar_rho, dim=1)
     del e
+    if w.dense_chunks >= 0:
+        A[:, w.dense_chunks * w.chunk:] = 0
     sp = spike_chunks(w, layer)
     if sp.numel():
         gs = _gen(w, layer, "spike", device)
