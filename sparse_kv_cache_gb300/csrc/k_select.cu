@@ -8,16 +8,21 @@
 // summary section 3.4, Steps 2-3 and "The temporal KV cache mechanism".
 // Algorithm 1: I = ArgTopK(-Min(S, dim=-1), o) picks the outliers.
 //
-// One 1024-thread CTA per (batch, KV head) unit.  Ordering by
+// One 1024-thread CTA per (batch, KV head) unit; a unit with more than 16K
+// chunks, when SMs are left over, runs on a thread-block cluster of up to 16
+// CTAs, each holding a contiguous slice of the unit's scores.  Ordering by
 // S2_j = max_g exp(z_gj - lse_g) equals ordering by v_j = max_g (z_gj - lse_g)
 // (exp is increasing), so the kernel ranks v_j.  The exact K-th largest value
 // T and the last index `jlast` taken among values equal to T are found with a
 // 2048-bin histogram over [min v, max v] (monotone binning), then an exact
 // rank among the <= 256 candidates of the boundary bin (or, for a crowded bin,
 // an exact 4-pass radix select on the order-preserving integer image of the
-// floats).  The selection {v > T} U {v == T, j <= jlast} has exactly K members
-// and gives equal scores to the lower index; it is written in ascending index
-// order by a two-pass warp-segmented compaction.
+// floats); the cluster form sums the range, the histogram and the radix
+// counts over its CTAs through distributed shared memory.  The selection
+// {v > T} U {v == T, j <= jlast} has exactly K members and gives equal scores
+// to the lower index; it is written in ascending index order by a ballot-based
+// compaction (per-warp counts of every row, one block-wide prefix sum, then each
+// taken score goes to its rank).
 #include <math_constants.h>
 
 #include <algorithm>
