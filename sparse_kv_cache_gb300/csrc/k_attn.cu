@@ -734,10 +734,12 @@ __global__ void __launch_bounds__(kD) k_attn_merge(AttnParams p, int ncta) {
     float M[G], L[G], A[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) { M[g] = -CUDART_INF_F; L[g] = 0.f; A[g] = 0.f; }
-    for (int c0 = 0; c0 < ncon; c0 += 2) {
-        float mm[2][G], ll[2][G], aa[2][G];   // two contributors' loads of all heads in flight
+    // contributors are combined in order, kMergeBatch at a time with all their loads in flight
+    constexpr int kMergeBatch = 8;
+    for (int c0 = 0; c0 < ncon; c0 += kMergeBatch) {
+        float mm[kMergeBatch][G], ll[kMergeBatch][G], aa[kMergeBatch][G];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < kMergeBatch; ++c) {
             const int st = aseg_start(cA + c0 + c, F, ncta) - u * nsegu;
             const float* pc = parts + static_cast<int64_t>(st > 0 ? st : 0) * G * kPartPitch;
             const bool on = c0 + c < ncon;
@@ -749,7 +751,7 @@ __global__ void __launch_bounds__(kD) k_attn_merge(AttnParams p, int ncta) {
             }
         }
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < kMergeBatch; ++c)
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 if (mm[c][g] == -CUDART_INF_F) continue;
