@@ -722,27 +722,20 @@ __global__ void __launch_bounds__((kAWarps + 2) * 32, 1) k_attn_tc(const __grid_
 // one CTA per unit, a thread per dimension, every contributor's (max, sum, p.V) of all
 // heads loaded at once.  Launched as a programmatic dependent of k_attn_tc: its CTAs may
 // become resident early and wait for the whole attention grid before reading.
-template <int G>
-__global__ void __launch_bounds__(kD) k_attn_merge(AttnParams p, int ncta) {
-    const int u = blockIdx.x, dim = threadIdx.x;
-    const int nsegu = p.nsplit, F = p.U * nsegu;
-    const int cA = acta_of(u * nsegu, F, ncta);
-    const int ncon = acta_of((u + 1) * nsegu - 1, F, ncta) - cA + 1;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (ncon <= 1) return;   // covered whole by one CTA, which wrote the output itself
-    const float* parts = p.part + static_cast<int64_t>(u) * nsegu * G * kPartPitch;
-    float M[G], L[G], A[G];
+// Combines contributors [0, ncon) of a unit in order, B at a time with all their loads in flight.
+template <int G, int B>
+__device__ __forceinline__ void merge_contribs(const float* parts, int cA, int ncon, int F, int ncta, int ubase,
+                                               int dim, float (&M)[G], float (&L)[G], float (&A)[G]) {
+    for (int c0 = 0; c0 < ncon; c0 += B) {
+        float mm[B][G], ll[B][G], aa[B][G];
 #pragma unroll
-    for (int g = 0; g < G; ++g) { M[g] = -CUDART_INF_F; L[g] = 0.f; A[g] = 0.f; }
-    // contributors are combined in order, kMergeBatch at a time with all their loads in flight
-    constexpr int kMergeBatch = 8;
-    for (int c0 = 0; c0 < ncon; c0 += kMergeBatch) {
-        float mm[kMergeBatch][G], ll[kMergeBatch][G], aa[kMergeBatch][G];
-#pragma unroll
-        for (int c = 0; c < kMergeBatch; ++c) {
-            const int st = aseg_start(cA + c0 + c, F, ncta) - u * nsegu;
-            const float* pc = parts + static_cast<int64_t>(st > 0 ? st : 0) * G * kPartPitch;
+        for (int c = 0; c < B; ++c) {
             const bool on = c0 + c < ncon;
+            const float* pc = parts;
+            if (on) {
+                const int st = aseg_start(cA + c0 + c, F, ncta) - ubase;
+                pc = parts + static_cast<int64_t>(st > 0 ? st : 0) * G * kPartPitch;
+            }
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 mm[c][g] = on ? __ldcg(pc + g * kPartPitch + kD) : -CUDART_INF_F;
@@ -751,7 +744,7 @@ __global__ void __launch_bounds__(kD) k_attn_merge(AttnParams p, int ncta) {
             }
         }
 #pragma unroll
-        for (int c = 0; c < kMergeBatch; ++c)
+        for (int c = 0; c < B; ++c)
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 if (mm[c][g] == -CUDART_INF_F) continue;
@@ -767,6 +760,24 @@ __global__ void __launch_bounds__(kD) k_attn_merge(AttnParams p, int ncta) {
                 }
             }
     }
+}
+
+template <int G>
+__global__ void __launch_bounds__(kD) k_attn_merge(AttnParams p, int ncta) {
+    const int u = blockIdx.x, dim = threadIdx.x;
+    const int nsegu = p.nsplit, F = p.U * nsegu;
+    const int cA = acta_of(u * nsegu, F, ncta);
+    const int ncon = acta_of((u + 1) * nsegu - 1, F, ncta) - cA + 1;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (ncon <= 1) return;   // covered whole by one CTA, which wrote the output itself
+    const float* parts = p.part + static_cast<int64_t>(u) * nsegu * G * kPartPitch;
+    float M[G], L[G], A[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) { M[g] = -CUDART_INF_F; L[g] = 0.f; A[g] = 0.f; }
+    // a unit split over many CTAs (a long context at a small batch) takes eight contributors
+    // per round trip; the usual two to four take two at a time
+    if (ncon <= 4) merge_contribs<G, 2>(parts, cA, ncon, F, ncta, u * nsegu, dim, M, L, A);
+    else merge_contribs<G, 8>(parts, cA, ncon, F, ncta, u * nsegu, dim, M, L, A);
 #pragma unroll
     for (int g = 0; g < G; ++g)
         static_cast<__nv_bfloat16*>(p.out)[(static_cast<int64_t>(u) * G + g) * kD + dim] = __float2bfloat16_rn(A[g] / L[g]);

@@ -45,7 +45,8 @@ struct SelShared {
     float red_f2[kWarps];
     int red_i[kWarps];
     int wpre[kWarps + 1];
-    float lse[8];
+    float lse[8];          // one-CTA form: log-sum-exp per query head
+    float2 lse_part[16];   // cluster form: (max, sum) of the log-sum-exp per warp of the first 16
     float vmin, vmax, T;
     int jlast, bstar, above, total;
     float cl_lo, cl_hi;   // cluster form: this CTA's score range and counts, read by the others
@@ -91,6 +92,38 @@ __device__ int block_exscan(int v, SelShared& sh, int* total) {
     if (total) *total = sh.wpre[kWarps];
     __syncthreads();
     return r;
+}
+
+// Sums of the int at `a` (and at `b`) over the first n CTAs of the cluster, the same offset in
+// each CTA's shared memory; four ranks' loads are in flight at a time.
+__device__ __forceinline__ int cluster_sum(const int* a, int n) {
+    int s = 0;
+    for (int r0 = 0; r0 < n; r0 += 4) {
+        int v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = r0 + i < n ? ld_cluster_s32(cluster_addr(a, r0 + i)) : 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s += v[i];
+    }
+    return s;
+}
+__device__ __forceinline__ void cluster_sum2(const int* a, const int* b, int n, int& sa, int& sb) {
+    sa = 0;
+    sb = 0;
+    for (int r0 = 0; r0 < n; r0 += 4) {
+        int va[4], vb[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const bool on = r0 + i < n;
+            va[i] = on ? ld_cluster_s32(cluster_addr(a, r0 + i)) : 0;
+            vb[i] = on ? ld_cluster_s32(cluster_addr(b, r0 + i)) : 0;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            sa += va[i];
+            sb += vb[i];
+        }
+    }
 }
 
 // Exact threshold of the k largest of vals[0..n) (ties to the lower index).
@@ -239,14 +272,19 @@ __device__ void topk_threshold_cl(const float* vals, int nl, int j0, int k, SelS
         if (lane == 0) { sh.cl_lo = lo; sh.cl_hi = hi; }
     }
     cluster_sync_all();   // every CTA's range is published; every candidate counter is zero
-    if (tid == 0) {
+    if (warp == 0) {
+        // lane r reads rank r's range (C <= 32)
         float L = CUDART_INF_F, Hh = -CUDART_INF_F;
-        for (int r = 0; r < C; ++r) {
-            L = fminf(L, ld_cluster_f32(cluster_addr(&sh.cl_lo, r)));
-            Hh = fmaxf(Hh, ld_cluster_f32(cluster_addr(&sh.cl_hi, r)));
+        if (lane < C) {
+            L = ld_cluster_f32(cluster_addr(&sh.cl_lo, lane));
+            Hh = ld_cluster_f32(cluster_addr(&sh.cl_hi, lane));
         }
-        sh.vmin = L;
-        sh.vmax = Hh;
+        L = warp_min(L);
+        Hh = warp_max(Hh);
+        if (lane == 0) {
+            sh.vmin = L;
+            sh.vmax = Hh;
+        }
     }
     __syncthreads();
     const float vmin = sh.vmin, vmax = sh.vmax;
@@ -267,11 +305,8 @@ __device__ void topk_threshold_cl(const float* vals, int nl, int j0, int k, SelS
     cluster_sync_all();   // every CTA's histogram is complete
     {
         const int b0 = kBins - 1 - 2 * tid, b1 = b0 - 1;
-        int h0 = 0, h1 = 0;
-        for (int r = 0; r < C; ++r) {
-            h0 += ld_cluster_s32(cluster_addr(&sh.hist[b0], r));
-            h1 += ld_cluster_s32(cluster_addr(&sh.hist[b1], r));
-        }
+        int h0, h1;
+        cluster_sum2(&sh.hist[b0], &sh.hist[b1], C, h0, h1);
         const int above = block_exscan(h0 + h1, sh, nullptr);
         if (above < k && k <= above + h0 + h1) {
             const bool first = above + h0 >= k;
@@ -332,13 +367,14 @@ __device__ void topk_threshold_cl(const float* vals, int nl, int j0, int k, SelS
             if ((key & mask) == prefix) atomicAdd(&sh.hist[(key >> shift) & 255], 1);
         }
         cluster_sync_all();   // every CTA's digit counts are complete
+        // digit d's count over the cluster, one thread per digit (the candidate slots are free here)
+        if (tid < 256) sh.cand_j[tid] = cluster_sum(&sh.hist[tid], C);
+        __syncthreads();
         if (tid == 0) {
             int c = 0, d = 255;
             for (; d > 0; --d) {
-                int hd = 0;
-                for (int r = 0; r < C; ++r) hd += ld_cluster_s32(cluster_addr(&sh.hist[d], r));
-                if (c + hd >= rem) break;
-                c += hd;
+                if (c + sh.cand_j[d] >= rem) break;
+                c += sh.cand_j[d];
             }
             sh.above = c;
             sh.bstar = d;
@@ -361,11 +397,7 @@ __device__ void topk_threshold_cl(const float* vals, int nl, int j0, int k, SelS
         sh.cl_cnt = t;
     }
     cluster_sync_all();   // every CTA's count of ties is published
-    if (tid == 0) {
-        int base = 0;
-        for (int r = 0; r < rank; ++r) base += ld_cluster_s32(cluster_addr(&sh.cl_cnt, r));
-        sh.above = base;
-    }
+    if (tid == 0) sh.above = cluster_sum(&sh.cl_cnt, rank);
     __syncthreads();
     const int base = sh.above;
     if (rem - 1 >= base && rem - 1 < base + sh.cl_cnt) {
@@ -468,7 +500,7 @@ __device__ __forceinline__ int lower_bound(const int32_t* a, int n, int x) {
 
 // ----------------------------------------------------------------- decode
 template <int G, bool CL>
-__global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
+__device__ __forceinline__ void select_decode(const SelectParams& p) {
     extern __shared__ __align__(16) uint8_t dsm[];
     __shared__ SelShared sh;
     // cluster form (CL): the unit's scores are split into C contiguous slices, one per CTA of a
@@ -489,9 +521,12 @@ __global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
     int32_t* sFree = sSlot + K;
     int32_t* sPid = sFree + K;       // previous step's selection (ascending) ...
     int32_t* sPslot = sPid + K;      // ... and its slots
-    if (crank == 0 && warp >= G) {
-        // work with no dependency on the scores, done while warps < G form the log-sum-exp
-        const int wt = tid - G * 32, nt = kSelThreads - G * 32;
+    // log-sum-exp warps: one per query head in the one-CTA form; in the cluster form 16, kWpg
+    // per head when the records need more than one round of loads
+    constexpr int kLseWarps = CL ? 16 : G, kWpg = 16 / G;
+    if (crank == 0 && warp >= kLseWarps) {
+        // work with no dependency on the scores, done while the first warps form the log-sum-exp
+        const int wt = tid - kLseWarps * 32, nt = kSelThreads - kLseWarps * 32;
         if (p.t > 0) {
             const int32_t* gp = p.prev_ids + static_cast<int64_t>(u) * K;
             const int32_t* gs = p.prev_slot + static_cast<int64_t>(u) * K;
@@ -533,19 +568,22 @@ __global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
         }
     }
 
-    // 1. log-sum-exp of every query head from the scoring runs' records
-    if (warp < G) {
-        const int np = p.nparts;
-        const int nrec = p.nru * np;
+    // 1. log-sum-exp of every query head from the scoring runs' records: wpg warps per head
+    // (kWpg when the records need more than one round of loads), each over an interleaved share
+    // of the records, combined after the barrier below
+    const int nrec = p.nru * p.nparts;
+    const int wpg = (CL && nrec > 4 * 32) ? kWpg : 1;
+    if (warp < wpg * G) {
+        const int g = warp % G, part = warp / G;
         const float2* rec = p.part + static_cast<int64_t>(u) * nrec * G;
         // running (max, sum) per lane over its records, four loads in flight at a time
         float m = -CUDART_INF_F, sx = 0.f;
-        for (int r0 = lane; r0 < nrec; r0 += 4 * 32) {
+        for (int r0 = part * 32 + lane; r0 < nrec; r0 += 4 * 32 * wpg) {
             float2 x[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int r = r0 + 32 * i;
-                x[i] = r < nrec ? rec[r * G + warp] : make_float2(-CUDART_INF_F, 0.f);
+                const int r = r0 + 32 * wpg * i;
+                x[i] = r < nrec ? rec[r * G + g] : make_float2(-CUDART_INF_F, 0.f);
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -560,14 +598,34 @@ __global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
         }
         const float M = warp_max(m);
         const float S = warp_sum(m == -CUDART_INF_F ? 0.f : sx * __expf(m - M));
-        if (lane == 0) sh.lse[warp] = M + __logf(S);
+        if (lane == 0) {
+            if constexpr (CL) sh.lse_part[warp] = make_float2(M, S);
+            else sh.lse[warp] = M + __logf(S);
+        }
     }
     if (u == 0 && crank == 0 && tid == 0 && p.sched) *p.sched = 0;   // the scoring kernel of this step is done
     __syncthreads();
     // 2. v_j = max_g (z_gj - lse_g)
     float lse[G];
 #pragma unroll
-    for (int g = 0; g < G; ++g) lse[g] = sh.lse[g];
+    for (int g = 0; g < G; ++g) {
+        if constexpr (!CL) {
+            lse[g] = sh.lse[g];
+            continue;
+        }
+        float M = sh.lse_part[g].x, S = sh.lse_part[g].y;
+        if (wpg > 1) {
+#pragma unroll
+            for (int q = 1; q < kWpg; ++q) M = fmaxf(M, sh.lse_part[q * G + g].x);
+            S = 0.f;
+#pragma unroll
+            for (int q = 0; q < kWpg; ++q) {
+                const float2 e = sh.lse_part[q * G + g];
+                if (e.x != -CUDART_INF_F) S += e.y * __expf(e.x - M);
+            }
+        }
+        lse[g] = M + __logf(S);
+    }
     const float* z = p.logits + (static_cast<int64_t>(u) * n + j0) * G;   // this CTA's slice
     float lo = CUDART_INF_F, hi = -CUDART_INF_F;
     if constexpr (G == 4) {
@@ -630,16 +688,8 @@ __global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
         for (int i = tid; i < mine; i += kSelThreads) sSel[i] = ids[j0 + sSel[i]];
         if (tid == 0) sh.cl_cnt = got;
         cluster_sync_all();
-        if (tid == 0) {
-            int base = 0, total = 0;
-            for (int r = 0; r < C; ++r) {
-                const int cr = ld_cluster_s32(cluster_addr(&sh.cl_cnt, r));
-                if (r < crank) base += cr;
-                total += cr;
-            }
-            sh.above = base;
-            sh.total = total;
-        }
+        if (tid == 0) sh.above = cluster_sum(&sh.cl_cnt, crank);
+        if (tid == 32) sh.total = cluster_sum(&sh.cl_cnt, C);
         __syncthreads();
         const int base = sh.above;
         if (crank != 0)
@@ -724,6 +774,18 @@ __global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
     }
 }
 
+// One CTA per unit.
+template <int G>
+__global__ void __launch_bounds__(kSelThreads) k_select_decode(SelectParams p) {
+    select_decode<G, false>(p);
+}
+
+// One cluster per unit (one CTA per SM: the full register file is available).
+template <int G>
+__global__ void __launch_bounds__(kSelThreads, 1) k_select_decode_cl(SelectParams p) {
+    select_decode<G, true>(p);
+}
+
 // ----------------------------------------------------------------- outliers (prefill)
 __global__ void __launch_bounds__(kSelThreads) k_select_outliers(SelectParams p) {
     extern __shared__ __align__(16) uint8_t dsm[];
@@ -758,10 +820,10 @@ int launch_select_decode(int dtype, const SelectParams& p, cudaStream_t s) {
     void (*fn)(SelectParams) = nullptr;    // one CTA per unit
     void (*fnc)(SelectParams) = nullptr;   // a cluster per unit
     switch (p.G) {
-        case 1: fn = k_select_decode<1, false>; fnc = k_select_decode<1, true>; break;
-        case 2: fn = k_select_decode<2, false>; fnc = k_select_decode<2, true>; break;
-        case 4: fn = k_select_decode<4, false>; fnc = k_select_decode<4, true>; break;
-        case 8: fn = k_select_decode<8, false>; fnc = k_select_decode<8, true>; break;
+        case 1: fn = k_select_decode<1>; fnc = k_select_decode_cl<1>; break;
+        case 2: fn = k_select_decode<2>; fnc = k_select_decode_cl<2>; break;
+        case 4: fn = k_select_decode<4>; fnc = k_select_decode_cl<4>; break;
+        case 8: fn = k_select_decode<8>; fnc = k_select_decode_cl<8>; break;
         default: return -1;
     }
     // A unit with more than kSelOneCta scores and SMs to spare is split over a cluster of C
