@@ -62,6 +62,8 @@ def parse():
     ap.add_argument("--share-storage", default="auto", choices=["auto", "yes", "no"],
                     help="reuse one layer's A/B/V for every layer (state stays per layer)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=0.0,
+                    help="--impl reference: oracle seconds per timed step (default: the run fits in ~2 minutes)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--microbatches", type=int, default=1,
                     help="split the batch into this many handles per layer, each on its own stream pair")
@@ -459,11 +461,7 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
         "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16+e5m2" if w.dtype == "fp8" else w.dtype,
         "data": "synthetic (seeded generator; Llama-3.1-8B attention shape)",
-        "config": {"workload": w.name, "layers": L, "batch_per_gpu": w.batch, "seq_len": w.seq_len,
-                   "n_kv_heads": w.n_kv_heads, "n_q_heads": w.n_q_heads, "head_dim": w.head_dim,
-                   "rank": w.rank, "chunk": w.chunk, "n_select": w.n_select, "n_outlier": w.n_outlier,
-                   "local_window": w.local_window, "v_place": w.v_place, "drift": w.drift,
-                   "new_keys": w.new_keys,
+        "config": {**workload_config(w, L),
                    "parallelism": f"replicas x{ws} (batch sharded, no collective)",
                    "microbatches": M,
                    "layers_share_input_storage": share,
@@ -492,6 +490,15 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
     if ws > 1:
         dist.destroy_process_group()
     return line
+
+
+def workload_config(w: Workload, layers: int) -> dict:
+    """The workload part of the JSON line's config, the same for both arms."""
+    return {"workload": w.name, "layers": layers, "batch_per_gpu": w.batch, "seq_len": w.seq_len,
+            "n_kv_heads": w.n_kv_heads, "n_q_heads": w.n_q_heads, "head_dim": w.head_dim,
+            "rank": w.rank, "chunk": w.chunk, "n_select": w.n_select, "n_outlier": w.n_outlier,
+            "local_window": w.local_window, "v_place": w.v_place, "drift": w.drift,
+            "new_keys": w.new_keys, "dtype": w.dtype}
 
 
 # ----------------------------------------------------------------------------- oracle arm
@@ -552,7 +559,7 @@ def run_reference(args, w: Workload, ws: int, rank: int):
     if rank != 0:
         return None
     K, W = args.steps, args.warmup
-    budget = max(0.5, min(10.0, 120.0 / max(1, K + W)))
+    budget = args.ref_budget if args.ref_budget > 0 else max(0.5, min(10.0, 120.0 / max(1, K + W)))
     o = OracleSample(w)
     for _ in range(W):
         o.timed_steps(budget / 4, cap=2)
@@ -564,7 +571,7 @@ def run_reference(args, w: Workload, ws: int, rank: int):
         "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1, "steps": K,
         "warmup": W, "ms_per_step": step_s * 1000.0, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generator)",
-        "config": {"workload": w.name, "layers": w.layers, "batch_per_gpu": w.batch, "seq_len": w.seq_len},
+        "config": {**workload_config(w, w.layers), "parallelism": "oracle on the host cores (rank 0 only)"},
         "cpu_baseline": {"value": v, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                          "sample": (f"each step: float64 oracle decode steps of one unit of layer 0 for about "
                                     f"{budget:.1f} s, scaled to {w.units} units x {w.layers} layers")},

@@ -1,11 +1,12 @@
-"""The benchmark's host logic on CPU: workload construction from the command line and the
-rule that reports the scorer's measured DRAM traffic only for the source it was measured on."""
+"""The benchmark's host logic on CPU: workload construction from the command line, the rule
+that reports the scorer's measured DRAM traffic only for the source it was measured on, and the
+reference arm (the float64 oracle timed on the host cores), which needs no GPU."""
 import sys
 
 import pytest
 
 import bench
-from workload import LLAMA_128K
+from workload import LLAMA_128K, TINY
 
 
 def _args(*argv):
@@ -56,3 +57,18 @@ def test_scorer_traffic_only_for_the_measured_source(monkeypatch):
     assert f8 == pytest.approx(bench.SCORE_TRAFFIC["fp8"]["bytes_per_unit"] * LLAMA_128K.units)
     assert bench.score_traffic_per_launch(LLAMA_128K.with_(dtype="f32")) is None                 # not captured
     assert bench.score_traffic_per_launch(LLAMA_128K.with_(seq_len=65536)) is None               # other length
+
+
+def test_reference_arm_prints_the_same_metric_and_workload():
+    args = _args("--impl", "reference", "--config", TINY.name, "--steps", "2", "--warmup", "1", "--ref-budget", "0.05")
+    w = bench.workload_from(args)
+    line = bench.run_reference(args, w, 1, 0)
+    assert line["impl"] == "reference"
+    assert (line["metric"], line["unit"], line["higher_is_better"]) == (bench.METRIC, bench.UNIT, True)
+    assert line["value"] > 0 and line["ms_per_step"] > 0
+    assert (line["steps"], line["warmup"]) == (2, 1)
+    # the workload keys are those the GPU arm reports for the same run
+    assert {k: line["config"][k] for k in bench.workload_config(w, w.layers)} == bench.workload_config(w, w.layers)
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": bench.UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert bench.run_reference(args, w, 2, 1) is None          # other ranks print nothing
