@@ -32,6 +32,12 @@ Readings where the pages are silent (each is also listed in the design notes):
 * ShadowKV+ (generated keys at rank r): the new key arrives pre-RoPE, over all
   H heads of its batch element, and is kept as k' Psi with Psi = B^T; attention
   uses each generated token's key rebuilt from that state, RoPE(a.B_h) at S+t.
+* FP8 storage (the summary's precision study runs ShadowKV in e5m2): landmarks
+  and values are held in e5m2 (nearest, ties to the even mantissa, saturating);
+  the query enters the score exactly, every kept key stays in bf16.
+* Pre-filling from exact keys (Algorithm 1 takes K and K_RoPE): when the keys
+  are given, landmarks, the min-cosine test and the outlier keys come from
+  RoPE(K); A and B serve the decode-time rebuild only.
 
 Parity pins: see ``tests/test_oracle_pins.py`` and ``tests/test_golden.py``.
 The selection scores' near-tie band is not pinned by the pages (no page prints
