@@ -5,6 +5,7 @@ import numpy as np
 import pytest
 
 from oracle import shadowkv_ref as ref
+from tests import test_golden as golden
 from tests import test_oracle_pins as pins
 
 
@@ -112,6 +113,60 @@ def _project_first_head_only(k_pre_b, B_b, storage=None):
 def _new_key_without_rope(a, B_bh, pos, base):
     return np.asarray(a, np.float64) @ np.asarray(B_bh, np.float64)
 
+
+def _rebuild_rope_one_late(A_rows, B_h, pos, base):
+    return ref.apply_rope(np.asarray(A_rows, np.float64) @ np.asarray(B_h, np.float64), np.asarray(pos) + 1, base)
+
+
+def _softmax_over_columns(x):
+    m = x.max(axis=0, keepdims=True)
+    e = np.exp(x - m)
+    return e / e.sum(axis=0, keepdims=True)
+
+
+def _bf16_truncate(x):
+    f = np.asarray(x, np.float64).astype(np.float32)
+    return (f.view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32).astype(np.float64)
+
+
+def _decode_without_append(st, q_group, k_new, v_new, A_b, B_bh, V_bh, k, C, base):
+    sel = ref.select_chunks(q_group, st.pre.landmarks, st.pre.ids, k)
+    hits, misses = ref.hit_miss(st.prev_sel, sel["sel"])
+    A_b = np.asarray(A_b, np.float64)
+    V_bh = np.asarray(V_bh, np.float64)
+    ts = ref.chunk_tokens(sel["sel"], C)
+    K = np.concatenate([st.pre.k_outlier, ref.rebuild_keys(A_b[ts], B_bh, ts, base), np.stack(st.pre.k_local)])
+    V = np.concatenate([st.pre.v_outlier, V_bh[ts], np.stack(st.pre.v_local)])
+    out = ref.attend(q_group, K, V)
+    st.prev_sel = sel["sel"]
+    st.steps += 1
+    return {"out": out, "sel": sel["sel"], "S2": sel["S2"], "ranked": sel["ranked"], "hits": hits, "misses": misses}
+
+
+def _attend_index_set_without_local(q_group, A_b, B_bh, V_bh, outlier_ids, sel_ids, k_local, v_local, C, base,
+                                    **kw):
+    return _orig_attend_on_index_set(q_group, A_b, B_bh, V_bh, outlier_ids, sel_ids, [], [], C, base, **kw)
+
+
+_orig_attend_on_index_set = ref.attend_on_index_set
+
+
+def _eqbw_all_misses(S, C, K, O, alpha, B_gpu, B_pcie):
+    return 2.0 * S * B_gpu / (S / C + 2.0 * (K + O) * C + K * C * B_gpu / B_pcie)
+
+
+def _eqbw_terms_single_kv(S, C, K, O, alpha, B_gpu, B_pcie):
+    return (S / C, (K + O) * C, (1.0 - alpha) * K * C * B_gpu / B_pcie)
+
+
+def _memory_savings_one_cache(S, M, C, K, O, r):
+    return S * M / (S * M / C + 2.0 * (K + O) * C + S * r + r * M)
+
+
+def _budget_without_outliers(K, O, C):
+    return K * C
+
+
 MUTANTS = [
     ("e5m2_round", _e5m2_ties_away, [pins.test_e5m2_round_hand_values]),
     ("apply_rope", _rope_wrong_sign, [pins.test_rope_closed_form_basis_vectors]),
@@ -131,6 +186,15 @@ MUTANTS = [
                                                    pins.test_plus_projection_brute_force]),
     ("new_token_key", _new_key_without_rope, [pins.test_plus_full_rank_equals_exact_new_keys]),
     ("prefill_unit", _prefill_ignores_exact_keys, [pins.test_exact_key_prefill_brute_force]),
+    ("rebuild_keys", _rebuild_rope_one_late, [pins.test_rebuild_is_rank_exact]),
+    ("softmax_rows", _softmax_over_columns, [pins.test_group_max_and_softmax_rows]),
+    ("bf16_round", _bf16_truncate, [pins.test_bf16_round_matches_torch]),
+    ("decode_step_unit", _decode_without_append, [pins.test_full_rank_full_budget_equals_dense_causal_attention]),
+    ("attend_on_index_set", _attend_index_set_without_local, [pins.test_attend_on_index_set_matches_decode_step]),
+    ("equivalent_bandwidth", _eqbw_all_misses, [golden.test_equivalent_bandwidth_worked_example]),
+    ("equivalent_bandwidth_terms", _eqbw_terms_single_kv, [golden.test_equivalent_bandwidth_terms]),
+    ("memory_savings", _memory_savings_one_cache, [golden.test_memory_savings_worked_example]),
+    ("sparse_budget_tokens", _budget_without_outliers, [golden.test_sparse_budget_tokens]),
 ]
 
 
