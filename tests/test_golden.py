@@ -38,6 +38,14 @@ def test_compression_ratio_worked_example():
     assert abs(ref.compression_ratio(i["s"], i["d"], i["r"]) - g["expected"]) <= g["abs_tol"]
 
 
+def test_compression_ratio_counts_stored_elements():
+    # the full key cache [s][d] against the factors A [s][r] and B [r][d], counted on real arrays
+    import numpy as np
+    for s, d, r in [(64, 16, 4), (100, 128, 8), (37, 5, 3)]:
+        K, A, B = np.zeros((s, d)), np.zeros((s, r)), np.zeros((r, d))
+        assert ref.compression_ratio(s, d, r) == pytest.approx(K.size / (A.size + B.size), rel=1e-15)
+
+
 def test_sparse_budget_tokens():
     g = GOLD["sparse_budget_tokens"]
     i = g["inputs"]

@@ -163,6 +163,10 @@ def _memory_savings_one_cache(S, M, C, K, O, r):
     return S * M / (S * M / C + 2.0 * (K + O) * C + S * r + r * M)
 
 
+def _compression_without_d(s, d, r):
+    return s * d / (r * s)
+
+
 def _budget_without_outliers(K, O, C):
     return K * C
 
@@ -195,6 +199,8 @@ MUTANTS = [
     ("equivalent_bandwidth_terms", _eqbw_terms_single_kv, [golden.test_equivalent_bandwidth_terms]),
     ("memory_savings", _memory_savings_one_cache, [golden.test_memory_savings_worked_example]),
     ("sparse_budget_tokens", _budget_without_outliers, [golden.test_sparse_budget_tokens]),
+    ("compression_ratio", _compression_without_d, [golden.test_compression_ratio_worked_example,
+                                                   golden.test_compression_ratio_counts_stored_elements]),
 ]
 
 
