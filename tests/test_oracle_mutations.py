@@ -163,6 +163,21 @@ def _memory_savings_one_cache(S, M, C, K, O, r):
     return S * M / (S * M / C + 2.0 * (K + O) * C + S * r + r * M)
 
 
+def _theta_without_two(d, base):
+    i = np.arange(d // 2, dtype=np.float64)
+    return np.power(float(base), -i / d)
+
+
+def _cosine_one_norm(x, y):
+    x = np.asarray(x, np.float64)
+    y = np.asarray(y, np.float64)
+    return (x * y).sum(axis=-1) / np.maximum((x * x).sum(axis=-1), 1e-12)
+
+
+def _values_like_keys(dtype):
+    return "bf16" if dtype == "fp8" else dtype
+
+
 def _compression_without_d(s, d, r):
     return s * d / (r * s)
 
@@ -199,6 +214,9 @@ MUTANTS = [
     ("equivalent_bandwidth_terms", _eqbw_terms_single_kv, [golden.test_equivalent_bandwidth_terms]),
     ("memory_savings", _memory_savings_one_cache, [golden.test_memory_savings_worked_example]),
     ("sparse_budget_tokens", _budget_without_outliers, [golden.test_sparse_budget_tokens]),
+    ("rope_theta", _theta_without_two, [pins.test_rope_closed_form_basis_vectors]),
+    ("cosine", _cosine_one_norm, [pins.test_min_cos_closed_forms]),
+    ("value_storage", _values_like_keys, [pins.test_fp8_storage_readings]),
     ("compression_ratio", _compression_without_d, [golden.test_compression_ratio_worked_example,
                                                    golden.test_compression_ratio_counts_stored_elements]),
 ]
