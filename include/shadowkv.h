@@ -267,6 +267,28 @@ int shadowkv_model(const skv_config* cfg, double alpha, int64_t t, double b_gpu_
  * out == NULL, SKV_ERR_OOM if the memory cannot be allocated and locked.
  */
 int shadowkv_host_alloc(size_t bytes, void** out);
+
+/*
+ * The same with a choice of host memory kind:
+ *   SKV_HOST_PINNED  page-locked memory (cudaHostAlloc); what shadowkv_host_alloc returns.
+ *   SKV_HOST_HUGE    pageable memory in the host's transparent huge pages (512 MiB on a
+ *                    kernel with 64 KiB base pages), which the GPU reads through the host's
+ *                    own page tables (Grace with NVLink-C2C; SKV_ERR_UNSUPPORTED elsewhere).
+ *                    The mapping is aligned to the huge-page size and advised for huge pages;
+ *                    the CUDA driver is told that its preferred location is the host and that
+ *                    the current device reads it, so it neither migrates nor splits the pages
+ *                    on the GPU's access counts.  Pages come into being when first written
+ *                    (fill it before the first shadowkv_prefill_index that reads it).  One
+ *                    translation then covers a whole huge page, and the value fetch's
+ *                    scattered 2 KB reads over tens of GiB keep their translations: measured
+ *                    for 32 x 2 GiB of values, about 170 GB/s against 125 GB/s from
+ *                    page-locked memory (link copy peak about 210 GB/s).
+ * SKV_ERR_INVALID for bytes == 0, out == NULL or an unknown kind; SKV_ERR_OOM if the memory
+ * cannot be had.  shadowkv_host_free releases either kind.
+ */
+#define SKV_HOST_PINNED 0
+#define SKV_HOST_HUGE   1
+int shadowkv_host_alloc_kind(size_t bytes, int kind, void** out);
 void shadowkv_host_free(void* p);
 
 /*
@@ -276,32 +298,54 @@ void shadowkv_host_free(void* p);
  * that runs under an allocator lock, or a hot path where an allocation (which
  * may synchronise the device) is forbidden.
  *
- * It computes what step 5 of shadowkv_decode_step computes, with the same
- * kernel: for each unit u (a batch element's KV head) and each of its G query
- * heads, out = softmax(q.K^T / sqrt(d)).V over the unit's outlier rows, then
- * its cache rows, then its first n_local_tokens local rows, all bf16, d = 128,
- * rows of a region contiguous per unit:
+ * It computes what step 5 of shadowkv_decode_step computes -- for each unit u
+ * (a batch element's KV head) and each of its G query heads,
+ * out = softmax(q.K^T / sqrt(d)).V over the unit's outlier rows, then its
+ * cache rows, then its first n_local_tokens local rows -- but with its own
+ * kernel (k_attn_bulk: 128-token splits staged by bulk copies, merged by the
+ * last CTA of each unit), not the decode step's persistent tensor-core kernel.
+ * All bf16, d = 128, rows of a region contiguous per unit:
  *   q         dev [units*group][128]                    (post-RoPE)
  *   k/v_outlier dev [units][n_outlier_tokens][128]      (may be NULL if 0 rows)
  *   k/v_cache dev [units][n_cache_tokens][128]          (may be NULL if 0 rows)
  *   k/v_local dev [units][local_capacity][128]
  *   out       dev [units*group][128]                    written
- * The caller owns every buffer.  The kernel's scratch (partial results of the
- * 128-token splits and one merge ticket per unit) lives in a fixed 16 MiB
- * array compiled into the library, which every GPU that loads the library
- * holds until the process exits.  A shape whose scratch does not fit --
- * units * ceil(rows / 128) * group * 528 bytes above 16 MiB - 64 KiB, or more
- * than 16384 units -- is rejected with SKV_ERR_INVALID; fp32 data with
- * SKV_ERR_UNSUPPORTED.  No cudaMalloc, cudaFree or other allocating call is
- * made.  The first call on a device resolves the array's device address for
- * that device (it must be the current device), so make that first call before
- * any stream capture.  Every call shares the one array and clears the merge
- * tickets itself (asynchronously, on `stream`); calls that overlap on the GPU
- * -- on different streams, or from different threads -- race on it, so
- * serialise them.
+ * The caller owns every buffer; each must be device memory (a host pointer is
+ * refused with SKV_ERR_INVALID before anything runs).
+ *
+ * Scratch: the partial results of the splits, one merge ticket per unit and an
+ * error word live in a fixed 16 MiB array compiled into the library, which
+ * every GPU that loads the library holds until the process exits.  Refused
+ * with SKV_ERR_INVALID: more than 16384 units; partials above
+ * 16 MiB - 64.25 KiB (units * ceil(rows / 128) * group * 528 bytes); or a unit
+ * whose merge state does not fit in one CTA's shared memory (64 KiB +
+ * 8 * ceil(rows / 128) * group bytes above the device's per-block limit, e.g.
+ * about 333K rows at group 8).  fp32 data: SKV_ERR_UNSUPPORTED.
+ *
+ * No cudaMalloc, cudaFree or other allocating call is made.  With CUDA's lazy
+ * module loading, though, the array itself comes into being when this part of
+ * the library is first used on a device -- by the first call here, or by the
+ * first decode step, whose attention kernels live in the same module.  A
+ * caller that gives all free HBM to a pool should therefore make a set-up call
+ * first: args->units == 0 launches nothing and only loads the array, resolves
+ * its device address for the current device and sets the kernel's
+ * shared-memory limit.  The first call on a device (set-up or not) does that
+ * set-up, with that device current; make it before any stream capture.  The
+ * address is resolved again if the device's context changes (after
+ * cudaDeviceReset).
+ *
+ * Every call shares the one array and clears the merge tickets itself
+ * (asynchronously, on `stream`); calls that overlap on the GPU -- on different
+ * streams, or from different threads -- race on it, so serialise them.
+ *
+ * Errors inside the kernel (a bounded wait for the staged rows that ran out,
+ * after about one second) are not seen by the call, which has returned
+ * already: the affected units' outputs are written as NaN, and the error is
+ * kept in the array's error word until shadowkv_sparse_attention_noalloc_status
+ * reads it.
  */
 typedef struct {
-    int32_t units;              /* b*H */
+    int32_t units;              /* b*H; 0: set-up only (see above) */
     int32_t group;              /* G in {1, 2, 4, 8} */
     int32_t dtype;              /* skv_dtype; only SKV_BF16 */
     int32_t n_outlier_tokens;   /* rows per unit in k/v_outlier */
@@ -318,6 +362,14 @@ typedef struct {
     void* out;
 } skv_attention_args;
 int shadowkv_sparse_attention_noalloc(const skv_attention_args* args, skv_stream stream);
+
+/*
+ * Status of the no-allocation calls made so far on the current device:
+ * synchronises `stream`, reads the error word of the fixed array and clears it.
+ * Returns SKV_OK, SKV_ERR_TIMEOUT (a kernel's wait ran out; those units' outputs
+ * are NaN), or SKV_ERR_CUDA.  Allocates nothing.  The pages have no counterpart.
+ */
+int shadowkv_sparse_attention_noalloc_status(skv_stream stream);
 
 void shadowkv_destroy(skv_layer* layer);   /* frees everything the handle owns; NULL ok */
 const char* shadowkv_strerror(int code);

@@ -5,5 +5,6 @@ ABI in include/shadowkv.h); this package is its ctypes binding.
 """
 from ._binding import (FIELDS, PHASES, SKV_BF16, SKV_F32, SKV_V_HBM, SKV_V_HOST,  # noqa: F401
                        HostBuffer, Layer, ShadowKVError, SkvConfig, load, make_config, model,
-                       sparse_attention_noalloc, strerror,
+                       sparse_attention_noalloc, sparse_attention_noalloc_setup,
+                       sparse_attention_noalloc_status, strerror,
                        validate_config)

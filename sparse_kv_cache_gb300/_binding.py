@@ -15,6 +15,7 @@ LIB_PATH = os.path.join(HERE, "libshadowkv.so")
 SKV_F32, SKV_BF16, SKV_FP8 = 0, 1, 2
 DTYPE_CODES = {"f32": SKV_F32, "bf16": SKV_BF16, "fp8": SKV_FP8}
 SKV_V_HBM, SKV_V_HOST = 0, 1
+HOST_KINDS = {"pinned": 0, "huge": 1}   # SKV_HOST_PINNED, SKV_HOST_HUGE
 PHASES = ("score", "select", "rebuild", "fetch", "attn")
 FIELDS = {
     "landmarks": 0, "chunk_ids": 1, "outlier_ids": 2, "min_cos": 3, "k_outlier": 4, "v_outlier": 5,
@@ -28,8 +29,9 @@ EXPORTED = ("shadowkv_validate_config", "shadowkv_prefill_index", "shadowkv_pref
             "shadowkv_decode_step",
             "shadowkv_stats", "shadowkv_reset_stats", "shadowkv_set_profiling",
             "shadowkv_export_size", "shadowkv_export", "shadowkv_model", "shadowkv_destroy",
-            "shadowkv_strerror", "shadowkv_version", "shadowkv_host_alloc", "shadowkv_host_free",
-            "shadowkv_sparse_attention_noalloc")
+            "shadowkv_strerror", "shadowkv_version", "shadowkv_host_alloc", "shadowkv_host_alloc_kind",
+            "shadowkv_host_free",
+            "shadowkv_sparse_attention_noalloc", "shadowkv_sparse_attention_noalloc_status")
 
 
 class SkvConfig(ctypes.Structure):
@@ -106,10 +108,14 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.shadowkv_version.argtypes = []
     lib.shadowkv_host_alloc.argtypes = [sz, ctypes.POINTER(vp)]
     lib.shadowkv_host_alloc.restype = i32
+    lib.shadowkv_host_alloc_kind.argtypes = [sz, i32, ctypes.POINTER(vp)]
+    lib.shadowkv_host_alloc_kind.restype = i32
     lib.shadowkv_host_free.argtypes = [vp]
     lib.shadowkv_host_free.restype = None
     lib.shadowkv_sparse_attention_noalloc.argtypes = [ctypes.POINTER(SkvAttentionArgs), vp]
     lib.shadowkv_sparse_attention_noalloc.restype = i32
+    lib.shadowkv_sparse_attention_noalloc_status.argtypes = [vp]
+    lib.shadowkv_sparse_attention_noalloc_status.restype = i32
     for name in ("shadowkv_validate_config", "shadowkv_prefill_index", "shadowkv_decode_step",
                  "shadowkv_stats", "shadowkv_reset_stats", "shadowkv_set_profiling",
                  "shadowkv_export", "shadowkv_model", "shadowkv_version"):
@@ -165,6 +171,17 @@ def sparse_attention_noalloc(q, k_outlier, v_outlier, k_cache, v_cache, k_local,
     return load().shadowkv_sparse_attention_noalloc(ctypes.byref(a), _stream(stream))
 
 
+def sparse_attention_noalloc_setup(stream=None) -> int:
+    """shadowkv_sparse_attention_noalloc with units = 0: the per-device set-up only."""
+    a = SkvAttentionArgs(units=0, group=1, dtype=SKV_BF16)
+    return load().shadowkv_sparse_attention_noalloc(ctypes.byref(a), _stream(stream))
+
+
+def sparse_attention_noalloc_status(stream=None) -> int:
+    """shadowkv_sparse_attention_noalloc_status: the kept kernel status, cleared on read."""
+    return load().shadowkv_sparse_attention_noalloc_status(_stream(stream))
+
+
 def _ptr(t) -> int | None:
     return None if t is None else t.data_ptr()
 
@@ -177,16 +194,19 @@ def _stream(s) -> int | None:
 
 
 class HostBuffer:
-    """Page-locked host memory from shadowkv_host_alloc, viewed as a CPU tensor."""
+    """Host memory for values from shadowkv_host_alloc_kind, viewed as a CPU tensor:
+    kind "pinned" (page-locked) or "huge" (transparent huge pages read through the
+    host's page tables)."""
 
-    def __init__(self, shape, dtype):
+    def __init__(self, shape, dtype, kind: str = "pinned"):
         import numpy as np
         import torch
-        self.shape, self.dtype = tuple(shape), dtype
+        self.shape, self.dtype, self.kind = tuple(shape), dtype, kind
         elem = torch.empty((), dtype=dtype).element_size()
         self.nbytes = int(np.prod(self.shape)) * elem
         p = ctypes.c_void_p()
-        _check(load().shadowkv_host_alloc(self.nbytes, ctypes.byref(p)), "shadowkv_host_alloc")
+        _check(load().shadowkv_host_alloc_kind(self.nbytes, HOST_KINDS[kind], ctypes.byref(p)),
+               "shadowkv_host_alloc_kind")
         self._p = p
         raw = (ctypes.c_uint8 * self.nbytes).from_address(p.value)
         self.tensor = torch.frombuffer(raw, dtype=torch.uint8).view(dtype).view(self.shape)

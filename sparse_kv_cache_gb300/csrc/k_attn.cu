@@ -298,6 +298,14 @@ __global__ void __launch_bounds__(128) k_attn_bulk(AttnParams p) {
     }
     if (!mbar_wait(&barV, 0)) { set_err(p.err, DEV_ERR_TIMEOUT, 602); s_fail = 1; }
     __syncthreads();
+    // A wait that ran out left shared memory incomplete: give the copies still in flight one
+    // more bounded wait before the CTA may leave, and publish a NaN partial so that the unit's
+    // output is NaN instead of a plausible wrong value (the error word says why).
+    const bool failed = s_fail != 0;
+    if (failed && tid == 0) {
+        mbar_wait(&barK, 0);
+        mbar_wait(&barV, 0);
+    }
 #pragma unroll
     for (int g = 0; g < G; ++g) Lsum[g] = red_l[0][g] + red_l[1][g] + red_l[2][g] + red_l[3][g];
 
@@ -333,10 +341,10 @@ __global__ void __launch_bounds__(128) k_attn_bulk(AttnParams p) {
 #pragma unroll
         for (int h = 0; h < 8; ++h) x += sRed[h * G * kD + o];
         const int g = o / kD, dim = o % kD;
-        mypart[g * kPartPitch + dim] = x;
+        mypart[g * kPartPitch + dim] = failed ? CUDART_NAN_F : x;
         if (dim == 0) {
-            mypart[g * kPartPitch + kD] = M[g];
-            mypart[g * kPartPitch + kD + 1] = Lsum[g];
+            mypart[g * kPartPitch + kD] = failed ? 0.f : M[g];
+            mypart[g * kPartPitch + kD + 1] = failed ? 1.f : Lsum[g];
         }
     }
     __threadfence();
@@ -868,29 +876,164 @@ int launch_attn(int dtype, const AttnParams& p, cudaStream_t s) {
 // server that carves every byte of HBM out of one pool at start-up, code that
 // runs under an allocator lock, or an integration that forbids cudaMalloc on
 // its hot path because an allocation may synchronise the device.  This entry
-// point serves them: it runs the same split-K attention kernel as the decode
-// step over key/value regions the caller provides, and keeps the kernel's
-// scratch -- the per-split partial results and the per-unit merge tickets --
-// in one fixed array compiled into this library instead of memory allocated
-// for a layer.  It calls no cudaMalloc, cudaFree or other allocating routine.
+// point serves them.  It runs k_attn_bulk, the bulk-copy split-K attention
+// kernel above (the decode step itself runs the persistent tensor-core form,
+// k_attn_tc, whose scratch lives with the layer), over key/value regions the
+// caller provides, and keeps that kernel's scratch -- the per-split partial
+// results, the per-unit merge tickets and an error word -- in one fixed array
+// compiled into this library instead of memory allocated for a layer.  It
+// calls no cudaMalloc, cudaFree or other allocating routine.
 namespace skv {
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;   // whole array: 16 MiB
 constexpr size_t kNoAllocTicketBytes = size_t(64) << 10;    // merge tickets of up to 16384 units
+constexpr size_t kNoAllocErrBytes = 256;                    // error word (code, where), then padding
+constexpr size_t kNoAllocPartOffset = kNoAllocTicketBytes + kNoAllocErrBytes;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Identifier of the calling thread's current context (0 if unknown): the array's address is
+// resolved again when it changes, e.g. after cudaDeviceReset made a new primary context.
+static unsigned long long current_ctx_id() {
+    static CtxGetCurrentFn get_cur = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static bool looked = false;
+    if (!looked) {
+        looked = true;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_cur = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+        cudaGetLastError();
+    }
+    CUcontext c = nullptr;
+    unsigned long long id = 0;
+    if (get_cur && get_id && get_cur(&c) == CUDA_SUCCESS && c && get_id(c, &id) == CUDA_SUCCESS) return id;
+    return 0;
+}
+
+struct NoAllocDevice {
+    void* addr = nullptr;              // the array's device address in that context
+    unsigned long long ctx = 0;        // context the address belongs to
+    int smem_limit = 0;                // dynamic shared memory a k_attn_bulk launch may ask for
+    bool attr_set[4] = {false, false, false, false};   // G = 1, 2, 4, 8: the shared-memory cap set
+};
 static std::mutex g_noalloc_mu;
-static void* g_noalloc_addr[256];   // per device: the array's device address, once resolved
+static NoAllocDevice g_noalloc_dev[256];
+
+static int g_index(int G) { return G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3; }
 
 template <int G>
-static int launch_bulk_with(const AttnParams& p, cudaStream_t s) { return launch_bulk<G>(p, s); }
+static cudaError_t bulk_func_attrs(int* static_smem) {
+    cudaFuncAttributes fa;
+    const cudaError_t e = cudaFuncGetAttributes(&fa, k_attn_bulk<G>);
+    *static_smem = e == cudaSuccess ? static_cast<int>(fa.sharedSizeBytes) : 0;
+    return e;
+}
+template <int G>
+static cudaError_t bulk_set_cap(int bytes) {
+    return cudaFuncSetAttribute(k_attn_bulk<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+// Per-device set-up, under g_noalloc_mu, with that device current: the array's address, the
+// shared-memory limit, and the kernels' dynamic shared-memory cap (set once per device and G).
+static int noalloc_setup(int dev, NoAllocDevice** out) {
+    NoAllocDevice& d = g_noalloc_dev[dev];
+    const unsigned long long ctx = current_ctx_id();
+    if (!d.addr || (ctx != 0 && ctx != d.ctx)) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return SKV_ERR_CUDA;
+        }
+        d = NoAllocDevice{};
+        d.addr = p;
+        d.ctx = current_ctx_id();
+        int optin = 0, st = 0, st_max = 0;
+        if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            bulk_func_attrs<1>(&st) != cudaSuccess || (st_max = st, bulk_func_attrs<2>(&st)) != cudaSuccess ||
+            (st_max = st > st_max ? st : st_max, bulk_func_attrs<4>(&st)) != cudaSuccess ||
+            (st_max = st > st_max ? st : st_max, bulk_func_attrs<8>(&st)) != cudaSuccess) {
+            cudaGetLastError();
+            d = NoAllocDevice{};
+            return SKV_ERR_CUDA;
+        }
+        st_max = st > st_max ? st : st_max;
+        d.smem_limit = optin - st_max;
+    }
+    *out = &d;
+    return SKV_OK;
+}
+
+// dynamic shared memory of one k_attn_bulk CTA: key and value rows, then the larger of the
+// score buffer and the merge state (a weight and a (max, sum) value per split and head)
+static int64_t bulk_smem_bytes(int64_t nsplit, int G) {
+    const int64_t scores = static_cast<int64_t>(kBSeg) * G * 4;
+    const int64_t merge = 2 * nsplit * G * 4;
+    return static_cast<int64_t>(2) * kBSeg * kD * 2 + (scores > merge ? scores : merge);
+}
+
+template <int G>
+static int launch_noalloc(const AttnParams& p, NoAllocDevice* d, int smem, cudaStream_t s) {
+    const int gi = g_index(G);
+    if (!d->attr_set[gi]) {
+        // the cap is the device's limit, so any shape accepted by the size checks launches
+        if (bulk_set_cap<G>(d->smem_limit) != cudaSuccess) {
+            cudaGetLastError();
+            return SKV_ERR_CUDA;
+        }
+        d->attr_set[gi] = true;
+    }
+    k_attn_bulk<G><<<dim3(p.nsplit, p.U), 128, smem, s>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return SKV_ERR_CUDA;
+    return SKV_OK;
+}
+
+static bool is_device_mem(const void* ptr) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
 }  // namespace skv
 
 extern "C" int shadowkv_sparse_attention_noalloc(const skv_attention_args* a, skv_stream stream) {
     using namespace skv;
     if (!a) return SKV_ERR_INVALID;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SKV_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= 256) return SKV_ERR_UNSUPPORTED;
+    if (a->units == 0) {   // set-up only
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        NoAllocDevice* d = nullptr;
+        int rc = noalloc_setup(dev, &d);
+        for (int G : {1, 2, 4, 8}) {
+            if (rc) break;
+            cudaError_t e = G == 1 ? bulk_set_cap<1>(d->smem_limit) : G == 2 ? bulk_set_cap<2>(d->smem_limit)
+                          : G == 4 ? bulk_set_cap<4>(d->smem_limit) : bulk_set_cap<8>(d->smem_limit);
+            if (e != cudaSuccess) {
+                cudaGetLastError();
+                rc = SKV_ERR_CUDA;
+            } else {
+                d->attr_set[g_index(G)] = true;
+            }
+        }
+        return rc;
+    }
     if (a->dtype != SKV_BF16) return SKV_ERR_UNSUPPORTED;
     const int G = a->group;
-    if (a->units < 1 || (G != 1 && G != 2 && G != 4 && G != 8)) return SKV_ERR_INVALID;
+    if (a->units < 0 || (G != 1 && G != 2 && G != 4 && G != 8)) return SKV_ERR_INVALID;
     if (a->n_outlier_tokens < 0 || a->n_cache_tokens < 0 || a->n_local_tokens < 1 ||
         a->n_local_tokens > a->local_capacity)
         return SKV_ERR_INVALID;
@@ -900,28 +1043,27 @@ extern "C" int shadowkv_sparse_attention_noalloc(const skv_attention_args* a, sk
     if (!a->q || !a->k_local || !a->v_local || !a->out) return SKV_ERR_INVALID;
     if ((a->n_outlier_tokens && (!a->k_outlier || !a->v_outlier)) || (a->n_cache_tokens && (!a->k_cache || !a->v_cache)))
         return SKV_ERR_INVALID;
+    // every region the kernel reads or writes must be device memory (the bulk copies cannot
+    // read pageable host memory); pointer queries allocate nothing
+    if (!is_device_mem(a->q) || !is_device_mem(a->out) || !is_device_mem(a->k_local) || !is_device_mem(a->v_local) ||
+        (a->n_outlier_tokens && (!is_device_mem(a->k_outlier) || !is_device_mem(a->v_outlier))) ||
+        (a->n_cache_tokens && (!is_device_mem(a->k_cache) || !is_device_mem(a->v_cache))))
+        return SKV_ERR_INVALID;
     const int64_t ntot = static_cast<int64_t>(a->n_outlier_tokens) + a->n_cache_tokens + a->n_local_tokens;
     const int64_t nsplit = (ntot + kBSeg - 1) / kBSeg;
     const int64_t part_bytes = static_cast<int64_t>(a->units) * nsplit * G * kPartPitch * 4;
     if (nsplit > (1 << 20) || static_cast<int64_t>(a->units) * 4 > static_cast<int64_t>(kNoAllocTicketBytes) ||
-        part_bytes > static_cast<int64_t>(kNoAllocScratchBytes - kNoAllocTicketBytes))
+        part_bytes > static_cast<int64_t>(kNoAllocScratchBytes - kNoAllocPartOffset))
         return SKV_ERR_INVALID;   // the shape needs more scratch than the fixed array holds
 
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return SKV_ERR_CUDA;
     void* base = nullptr;
-    {
-        std::lock_guard<std::mutex> lock(g_noalloc_mu);
-        if (!g_noalloc_addr[dev]) {
-            void* p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
-                cudaGetLastError();
-                return SKV_ERR_CUDA;
-            }
-            g_noalloc_addr[dev] = p;
-        }
-        base = g_noalloc_addr[dev];
-    }
+    NoAllocDevice* d = nullptr;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    int rc = noalloc_setup(dev, &d);
+    if (rc) return rc;
+    base = d->addr;
+    const int64_t smem = bulk_smem_bytes(nsplit, G);
+    if (smem > d->smem_limit) return SKV_ERR_INVALID;   // the merge state does not fit in shared memory
     // the merge tickets must start at zero; the partials are fully overwritten
     if (cudaMemsetAsync(base, 0, static_cast<size_t>(a->units) * 4, stream) != cudaSuccess) {
         cudaGetLastError();
@@ -934,16 +1076,41 @@ extern "C" int shadowkv_sparse_attention_noalloc(const skv_attention_args* a, sk
     p.k_loc = a->k_local; p.v_loc = a->v_local; p.n_loc = a->n_local_tokens; p.loc_cap = a->local_capacity;
     p.out = a->out;
     p.counter = static_cast<int*>(base);
-    p.part = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + kNoAllocTicketBytes);
+    p.err = reinterpret_cast<int*>(static_cast<unsigned char*>(base) + kNoAllocTicketBytes);
+    p.part = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + kNoAllocPartOffset);
     p.nsplit = static_cast<int>(nsplit);
     p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(kD)));
-    p.G = G; p.U = a->units; p.err = nullptr;
-    int rc = -1;
+    p.G = G; p.U = a->units;
+    const int sm = static_cast<int>(smem);
     switch (G) {
-        case 1: rc = launch_bulk_with<1>(p, stream); break;
-        case 2: rc = launch_bulk_with<2>(p, stream); break;
-        case 4: rc = launch_bulk_with<4>(p, stream); break;
-        case 8: rc = launch_bulk_with<8>(p, stream); break;
+        case 1: return launch_noalloc<1>(p, d, sm, stream);
+        case 2: return launch_noalloc<2>(p, d, sm, stream);
+        case 4: return launch_noalloc<4>(p, d, sm, stream);
+        default: return launch_noalloc<8>(p, d, sm, stream);
     }
-    return rc == 0 ? SKV_OK : SKV_ERR_CUDA;
+}
+
+extern "C" int shadowkv_sparse_attention_noalloc_status(skv_stream stream) {
+    using namespace skv;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SKV_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= 256) return SKV_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    NoAllocDevice* d = nullptr;
+    int rc = noalloc_setup(dev, &d);
+    if (rc) return rc;
+    int e[2] = {0, 0};
+    unsigned char* w = static_cast<unsigned char*>(d->addr) + kNoAllocTicketBytes;
+    if (cudaStreamSynchronize(stream) != cudaSuccess ||
+        cudaMemcpyAsync(e, w, sizeof(e), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaMemsetAsync(w, 0, sizeof(e), stream) != cudaSuccess || cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SKV_ERR_CUDA;
+    }
+    if (e[0] == DEV_ERR_TIMEOUT) return SKV_ERR_TIMEOUT;
+    if (e[0] != 0) return SKV_ERR_DEVICE_BOUNDS;
+    return SKV_OK;
 }

@@ -171,3 +171,11 @@ def make_layer(w: Workload, layer: int, device="cpu"):
     """All prefill inputs of one layer: dict(A, B, V) in storage dtype on ``device``."""
     return {"A": make_A(w, layer, device), "B": make_B(w, layer, device),
             "V": make_V(w, layer, device)}
+
+
+def make_normal(shape, seed: int, dtype=torch.bfloat16, device="cpu") -> torch.Tensor:
+    """N(0,1) draws of a given shape from a generator seeded with ``seed`` (CPU stream),
+    rounded to ``dtype``: plain attention regions for tests of the attention call alone."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    return torch.randn(tuple(shape), generator=g, dtype=torch.float32).to(dtype).to(device)
