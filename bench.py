@@ -67,6 +67,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--microbatches", type=int, default=1,
                     help="split the batch into this many handles per layer, each on its own stream pair")
+    ap.add_argument("--host-mem", default="pinned", choices=["pinned", "huge"],
+                    help="host values: page-locked memory, or transparent huge pages read through the host page tables")
     ap.add_argument("--single-stream", action="store_true",
                     help="run the value fetch on the main stream too (per-kernel timing without overlap)")
     return ap.parse_args()
@@ -136,6 +138,20 @@ def measured_peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+def thp_counters() -> dict:
+    """Huge-page split and migration counters of the host kernel (/proc/vmstat)."""
+    keys = ("thp_split_pmd", "thp_split_page", "thp_fault_alloc", "pgmigrate_success")
+    out = {}
+    try:
+        for line in open("/proc/vmstat"):
+            k, _, v = line.partition(" ")
+            if k in keys:
+                out[k] = int(v)
+    except OSError:
+        pass
+    return out
 
 
 def mem_available_gb() -> float:
@@ -221,6 +237,7 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
         share = mem_available_gb() < 1.3 * L * v_bytes / 1e9 + 16
     n_data = 1 if share else L
 
+    thp0 = thp_counters()
     M = max(1, args.microbatches)
     if w.batch % M:
         raise SystemExit(f"batch {w.batch} is not a multiple of --microbatches {M}")
@@ -229,7 +246,7 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
     if w.v_place == "host":
         # one page-locked arena for every layer's values (large allocations keep GPU translations few)
         per = w.batch * w.n_kv_heads * w.seq_len * w.head_dim
-        arena = skv.HostBuffer((n_data * per,), vdt)
+        arena = skv.HostBuffer((n_data * per,), vdt, kind=args.host_mem)
     # one (main, side) stream pair per micro-batch; the value fetch (link-bound) goes first
     mains = [torch.cuda.Stream(dev) for _ in range(M)]
     sides = [torch.cuda.Stream(dev, priority=-10) for _ in range(M)]
@@ -444,6 +461,7 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
             "eq_bandwidth_gbs": mdl["eq_bandwidth_gbs"], "t_pred_ms_per_step": t_pred_ms,
             "t_meas_ms_per_step": ms / K, "meas_over_pred": (ms / K) / t_pred_ms}
 
+    thp1 = thp_counters()
     st_all = [lay.stats(check=False) for lay in layers]
     dev_err = [s["device_error"] for s in st_all if s["device_error"]]
     for lay in layers:
@@ -465,7 +483,10 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
                    "parallelism": f"replicas x{ws} (batch sharded, no collective)",
                    "microbatches": M,
                    "layers_share_input_storage": share,
-                   "host_values": "one page-locked arena (shadowkv_host_alloc)" if w.v_place == "host" else None,
+                   "host_values": ({"pinned": "one page-locked arena (shadowkv_host_alloc_kind, SKV_HOST_PINNED)",
+                                    "huge": "one arena of transparent huge pages read through the host page tables "
+                                            "(shadowkv_host_alloc_kind, SKV_HOST_HUGE)"}[args.host_mem]
+                                   if w.v_place == "host" else None),
                    "l2": "inputs larger than L2 (landmarks of one layer exceed 129 MB)"},
         "hbm_gbs": hbm_per_step / (step_ms * 1e-3) / 1e9,
         "hbm_frac_of_8tbs": hbm_per_step / 8e12 / (step_ms * 1e-3),
@@ -482,6 +503,7 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
         "e2e": e2e,
         "gpu_launches": launches,
         "setup_s": setup_s,
+        "host_thp_counters_delta": {k: thp1.get(k, 0) - thp0.get(k, 0) for k in thp1},
     }
     if dev_err:
         line["device_error"] = dev_err[0]

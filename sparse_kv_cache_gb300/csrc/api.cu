@@ -5,12 +5,15 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <sys/mman.h>
+
 #include <algorithm>
 #include <array>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -33,6 +36,23 @@ int fault_oom_at() {
     if (!e || std::strncmp(e, "oom", 3) != 0) return 0;
     if (e[3] == ':') return std::max(1, std::atoi(e + 4));
     return 1;
+}
+
+// huge-page host memory handed out by shadowkv_host_alloc_kind: (user pointer, mapping)
+struct HostMap { void* user; void* raw; size_t len; };
+std::mutex g_host_mu;
+std::vector<HostMap> g_host_maps;
+
+// size of the host's transparent huge pages (512 MiB with 64 KiB base pages, 2 MiB with 4 KiB)
+size_t host_huge_page_bytes() {
+    size_t v = 0;
+    if (FILE* f = std::fopen("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", "r")) {
+        unsigned long long x = 0;
+        if (std::fscanf(f, "%llu", &x) == 1) v = static_cast<size_t>(x);
+        std::fclose(f);
+    }
+    if (v < (size_t(2) << 20) || (v & (v - 1))) v = size_t(2) << 20;
+    return v;
 }
 
 int es_of(int dtype) { return dtype == SKV_F32 ? 4 : 2; }   // A, B, q, keys, out
@@ -805,20 +825,72 @@ int shadowkv_export(skv_layer* h, int field, void* dst, size_t bytes, skv_stream
     return SKV_OK;
 }
 
-int shadowkv_host_alloc(size_t bytes, void** out) {
+int shadowkv_host_alloc(size_t bytes, void** out) { return shadowkv_host_alloc_kind(bytes, SKV_HOST_PINNED, out); }
+
+int shadowkv_host_alloc_kind(size_t bytes, int kind, void** out) {
     if (!out || bytes == 0) return SKV_ERR_INVALID;
     *out = nullptr;
-    void* p = nullptr;
-    if (cudaHostAlloc(&p, bytes, cudaHostAllocPortable | cudaHostAllocMapped) != cudaSuccess || !p) {
+    if (kind == SKV_HOST_PINNED) {
+        void* p = nullptr;
+        if (cudaHostAlloc(&p, bytes, cudaHostAllocPortable | cudaHostAllocMapped) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return SKV_ERR_OOM;
+        }
+        *out = p;
+        return SKV_OK;
+    }
+    if (kind != SKV_HOST_HUGE) return SKV_ERR_INVALID;
+    // pageable memory in transparent huge pages, read by the GPU through the host's page
+    // tables: needs a device that does that (Grace with NVLink-C2C)
+    int dev = 0, ats = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&ats, cudaDevAttrPageableMemoryAccessUsesHostPageTables, dev) != cudaSuccess) {
         cudaGetLastError();
-        return SKV_ERR_OOM;
+        return SKV_ERR_CUDA;
+    }
+    if (!ats) return SKV_ERR_UNSUPPORTED;
+    const size_t hp = host_huge_page_bytes();
+    if (bytes > SIZE_MAX - 2 * hp) return SKV_ERR_INVALID;
+    const size_t len = (bytes + hp - 1) / hp * hp;
+    void* raw = mmap(nullptr, len + hp, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS | MAP_NORESERVE, -1, 0);
+    if (raw == MAP_FAILED) return SKV_ERR_OOM;
+    void* p = reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(raw) + hp - 1) / hp * hp);
+    // huge pages: one translation covers a whole page, so the fetch's scattered reads over a
+    // span of tens of GiB keep their translations; preferred location host: the driver never
+    // migrates (and so never splits) these pages toward the GPU on access counts
+    cudaMemLocation host{};
+    host.type = cudaMemLocationTypeHost;
+    host.id = 0;
+    cudaMemLocation gpu{};
+    gpu.type = cudaMemLocationTypeDevice;
+    gpu.id = dev;
+    if (madvise(p, len, MADV_HUGEPAGE) != 0 ||
+        cudaMemAdvise(p, len, cudaMemAdviseSetPreferredLocation, host) != cudaSuccess ||
+        cudaMemAdvise(p, len, cudaMemAdviseSetAccessedBy, gpu) != cudaSuccess) {
+        cudaGetLastError();
+        munmap(raw, len + hp);
+        return SKV_ERR_CUDA;
+    }
+    {
+        std::lock_guard<std::mutex> lock(g_host_mu);
+        g_host_maps.push_back({p, raw, len + hp});
     }
     *out = p;
     return SKV_OK;
 }
 
 void shadowkv_host_free(void* p) {
-    if (p) cudaFreeHost(p);
+    if (!p) return;
+    {
+        std::lock_guard<std::mutex> lock(g_host_mu);
+        for (size_t i = 0; i < g_host_maps.size(); ++i)
+            if (g_host_maps[i].user == p) {
+                munmap(g_host_maps[i].raw, g_host_maps[i].len);
+                g_host_maps.erase(g_host_maps.begin() + static_cast<long>(i));
+                return;
+            }
+    }
+    cudaFreeHost(p);
 }
 
 void shadowkv_destroy(skv_layer* h) {

@@ -57,8 +57,9 @@ class LayerRun:
         V = make_V(w, layer, gen_device)
         q, kn, vn = make_decode_inputs(w, layer, steps, gen_device)
         self.A_d, self.B_d = A.to(dev), B.to(dev)
-        if w.v_place == "host" and host_alloc == "arena":
-            self.V_buf = skv.HostBuffer((V.numel() + 64,), V.dtype)   # page-locked, via the library
+        if w.v_place == "host" and host_alloc in ("arena", "huge"):
+            # page-locked ("arena") or huge-page ("huge") host memory from the library
+            self.V_buf = skv.HostBuffer((V.numel() + 64,), V.dtype, kind="huge" if host_alloc == "huge" else "pinned")
             self.V_buf.fill_from(V, 64)
             self.V_arg = self.V_buf.slice(64, V.shape)     # an interior slice, as the bench uses
             self.V_cpu = self.V_arg

@@ -44,6 +44,12 @@ def test_bf16_host_arena_values():
     run_and_check(SMALL_BF16.with_(v_place="host", seed=14), 4, host_alloc="arena")
 
 
+def test_bf16_host_huge_page_values():
+    # huge-page pageable memory from shadowkv_host_alloc_kind(SKV_HOST_HUGE), read through the
+    # host page tables, passed as an interior slice
+    run_and_check(SMALL_BF16.with_(v_place="host", seed=15), 4, host_alloc="huge")
+
+
 def test_full_budget_selects_every_chunk():
     w = SMALL_BF16.with_(seq_len=1024, n_outlier=4, batch=1, seed=13)
     w = w.with_(n_select=w.n_selectable)
