@@ -173,6 +173,19 @@ int shadowkv_prefill_index_keys(const skv_config* cfg, const void* A, const void
 int shadowkv_decode_step(skv_layer* layer, const void* q, const void* k_new, const void* v_new,
                          void* out, int32_t* sel_out, skv_stream main, skv_stream side);
 
+/*
+ * Micro-batch pipelining.  A caller that splits its batch into independent
+ * handles per layer (micro-batches on their own streams) can let one
+ * micro-batch's value fetch overlap another's landmark scoring: the fetch
+ * moves data over the host link, the scoring reads HBM.  `event` (a
+ * cudaEvent_t the caller owns, or NULL to stop) is recorded on the main stream
+ * of every later decode step of this layer right after its selection, when
+ * the step's miss list is final; the caller makes the next micro-batch's
+ * stream wait for it before that micro-batch's decode step.  The library
+ * keeps no other reference to the event.
+ */
+int shadowkv_set_select_event(skv_layer* layer, void* event);
+
 /* Phases timed when profiling is on (CUDA events on the launching stream). */
 #define SKV_PH_SCORE   0
 #define SKV_PH_SELECT  1
@@ -275,9 +288,8 @@ int shadowkv_host_alloc(size_t bytes, void** out);
  *                    kernel with 64 KiB base pages), which the GPU reads through the host's
  *                    own page tables (Grace with NVLink-C2C; SKV_ERR_UNSUPPORTED elsewhere).
  *                    The mapping is aligned to the huge-page size and advised for huge pages;
- *                    the CUDA driver is told that its preferred location is the host and that
- *                    the current device reads it, so it neither migrates nor splits the pages
- *                    on the GPU's access counts.  Pages come into being when first written
+ *                    the CUDA driver is told that its preferred location is the host, so it
+ *                    does not migrate (and split) the pages on the GPU's access counts.  Pages come into being when first written
  *                    (fill it before the first shadowkv_prefill_index that reads it).  One
  *                    translation then covers a whole huge page, and the value fetch's
  *                    scattered 2 KB reads over tens of GiB keep their translations: measured
@@ -289,6 +301,20 @@ int shadowkv_host_alloc(size_t bytes, void** out);
 #define SKV_HOST_PINNED 0
 #define SKV_HOST_HUGE   1
 int shadowkv_host_alloc_kind(size_t bytes, int kind, void** out);
+
+/*
+ * Puts split huge pages of [p, p + bytes) -- inside one SKV_HOST_HUGE allocation -- back
+ * together (madvise MADV_COLLAPSE, Linux 6.1+; a page that is whole costs nothing).  Measured
+ * on a 64 GiB arena: about ten of its 128 pages split while the layers were pre-filled, and a
+ * split page costs the fetch a translation per 64 KiB instead of per 512 MiB.
+ * shadowkv_prefill_index repairs the layer's own values before it returns, and while any
+ * SKV_HOST_HUGE allocation exists a library thread watches the host's split count
+ * (/proc/vmstat thp_split_pmd, every 5 ms) and repairs every such allocation when it moves.
+ * A caller may also repair a range itself, e.g. after its warm-up.  Synchronous.
+ * SKV_ERR_INVALID if the range is not inside such an allocation, SKV_ERR_UNSUPPORTED if the
+ * host kernel lacks the call, SKV_ERR_OOM if no huge page could be had.
+ */
+int shadowkv_host_repair(void* p, size_t bytes);
 void shadowkv_host_free(void* p);
 
 /*
@@ -370,6 +396,23 @@ int shadowkv_sparse_attention_noalloc(const skv_attention_args* args, skv_stream
  * are NaN), or SKV_ERR_CUDA.  Allocates nothing.  The pages have no counterpart.
  */
 int shadowkv_sparse_attention_noalloc_status(skv_stream stream);
+
+/*
+ * Measurement aid, not from the pages: the rate of the decode step's value
+ * fetch on its own.  Reads n_chunks distinct random chunks of chunk_bytes
+ * (1024, 2048 or 4096: one chunk of C = 8 rows of e5m2, bf16 or fp32 values)
+ * spread over [src, src + bytes) -- host memory the GPU reads in place, or
+ * device memory -- into device scratch with the fetch kernel, in address
+ * order as the decode step reads its miss lists, on `stream`, reps + 1 times
+ * (the first untimed).  fresh = 0 reads the same chunks every time (the GPU's
+ * translations of them are warm after the first); fresh = 1 draws new chunks
+ * for every repetition, as successive layers' fetches do.  *gbs_out = chunk
+ * bytes per second of the fastest timed repetition (CUDA events).  Allocates
+ * and frees its own device scratch and synchronises `stream`.
+ * SKV_ERR_INVALID for bad sizes or a null or misaligned src.
+ */
+int shadowkv_fetch_probe(const void* src, size_t bytes, int64_t n_chunks, int chunk_bytes, uint64_t seed,
+                         int reps, int fresh, skv_stream stream, double* gbs_out);
 
 void shadowkv_destroy(skv_layer* layer);   /* frees everything the handle owns; NULL ok */
 const char* shadowkv_strerror(int code);

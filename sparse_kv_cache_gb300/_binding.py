@@ -28,10 +28,11 @@ ERRORS = {0: "OK", -1: "INVALID", -2: "OOM", -3: "NOT_PINNED", -4: "CUDA", -5: "
 EXPORTED = ("shadowkv_validate_config", "shadowkv_prefill_index", "shadowkv_prefill_index_keys",
             "shadowkv_decode_step",
             "shadowkv_stats", "shadowkv_reset_stats", "shadowkv_set_profiling",
-            "shadowkv_export_size", "shadowkv_export", "shadowkv_model", "shadowkv_destroy",
+            "shadowkv_set_select_event", "shadowkv_export_size", "shadowkv_export", "shadowkv_model", "shadowkv_destroy",
             "shadowkv_strerror", "shadowkv_version", "shadowkv_host_alloc", "shadowkv_host_alloc_kind",
-            "shadowkv_host_free",
-            "shadowkv_sparse_attention_noalloc", "shadowkv_sparse_attention_noalloc_status")
+            "shadowkv_host_repair", "shadowkv_host_free",
+            "shadowkv_sparse_attention_noalloc", "shadowkv_sparse_attention_noalloc_status",
+            "shadowkv_fetch_probe")
 
 
 class SkvConfig(ctypes.Structure):
@@ -96,6 +97,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.shadowkv_stats.argtypes = [vp, ctypes.POINTER(SkvStats)]
     lib.shadowkv_reset_stats.argtypes = [vp]
     lib.shadowkv_set_profiling.argtypes = [vp, i32]
+    lib.shadowkv_set_select_event.argtypes = [vp, vp]
     lib.shadowkv_export_size.argtypes = [vp, i32]
     lib.shadowkv_export_size.restype = i64
     lib.shadowkv_export.argtypes = [vp, i32, vp, sz, vp]
@@ -110,15 +112,20 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.shadowkv_host_alloc.restype = i32
     lib.shadowkv_host_alloc_kind.argtypes = [sz, i32, ctypes.POINTER(vp)]
     lib.shadowkv_host_alloc_kind.restype = i32
+    lib.shadowkv_host_repair.argtypes = [vp, sz]
+    lib.shadowkv_host_repair.restype = i32
     lib.shadowkv_host_free.argtypes = [vp]
     lib.shadowkv_host_free.restype = None
     lib.shadowkv_sparse_attention_noalloc.argtypes = [ctypes.POINTER(SkvAttentionArgs), vp]
     lib.shadowkv_sparse_attention_noalloc.restype = i32
     lib.shadowkv_sparse_attention_noalloc_status.argtypes = [vp]
+    lib.shadowkv_fetch_probe.argtypes = [vp, sz, i64, i32, ctypes.c_uint64, i32, i32, vp,
+                                         ctypes.POINTER(ctypes.c_double)]
+    lib.shadowkv_fetch_probe.restype = i32
     lib.shadowkv_sparse_attention_noalloc_status.restype = i32
     for name in ("shadowkv_validate_config", "shadowkv_prefill_index", "shadowkv_decode_step",
                  "shadowkv_stats", "shadowkv_reset_stats", "shadowkv_set_profiling",
-                 "shadowkv_export", "shadowkv_model", "shadowkv_version"):
+                 "shadowkv_set_select_event", "shadowkv_export", "shadowkv_model", "shadowkv_version"):
         getattr(lib, name).restype = i32
     _lib = lib
     return lib
@@ -182,6 +189,16 @@ def sparse_attention_noalloc_status(stream=None) -> int:
     return load().shadowkv_sparse_attention_noalloc_status(_stream(stream))
 
 
+def fetch_probe(src_ptr: int, nbytes: int, n_chunks: int, chunk_bytes: int = 2048, seed: int = 1,
+                reps: int = 3, fresh: bool = False, stream=None) -> float:
+    """shadowkv_fetch_probe: GB/s of the fetch kernel on random chunks of [src, src + nbytes)
+    (fresh: new chunks for every repetition)."""
+    g = ctypes.c_double()
+    _check(load().shadowkv_fetch_probe(src_ptr, nbytes, n_chunks, chunk_bytes, seed, reps, 1 if fresh else 0,
+                                       _stream(stream), ctypes.byref(g)), "shadowkv_fetch_probe")
+    return g.value
+
+
 def _ptr(t) -> int | None:
     return None if t is None else t.data_ptr()
 
@@ -219,6 +236,10 @@ class HostBuffer:
         flat = self.tensor.view(-1)
         s = src.contiguous().view(-1)
         flat[offset_elems:offset_elems + s.numel()].copy_(s)
+
+    def repair(self) -> int:
+        """shadowkv_host_repair over the whole buffer (huge-page kind); returns the status."""
+        return load().shadowkv_host_repair(self._p, self.nbytes)
 
     def slice(self, offset_elems: int, shape):
         """A view of part of the buffer (data_ptr() gives its address)."""
@@ -287,6 +308,14 @@ class Layer:
 
     def set_profiling(self, on: bool):
         _check(load().shadowkv_set_profiling(self._h, 1 if on else 0), "shadowkv_set_profiling")
+
+    def set_select_event(self, event):
+        """Record ``event`` (a torch.cuda.Event, or None to stop) after each step's selection."""
+        if event is not None and not event.cuda_event:
+            import torch
+            event.record(torch.cuda.current_stream())   # torch creates its events on first record
+        _check(load().shadowkv_set_select_event(self._h, None if event is None else event.cuda_event),
+               "shadowkv_set_select_event")
 
     def export_size(self, field: str) -> int:
         return load().shadowkv_export_size(self._h, FIELDS[field])

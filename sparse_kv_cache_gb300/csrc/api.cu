@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <errno.h>
 #include <sys/mman.h>
 
 #include <algorithm>
@@ -13,8 +14,11 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
+#include <chrono>
 #include <mutex>
 #include <new>
+#include <thread>
 #include <vector>
 
 
@@ -42,6 +46,74 @@ int fault_oom_at() {
 struct HostMap { void* user; void* raw; size_t len; };
 std::mutex g_host_mu;
 std::vector<HostMap> g_host_maps;
+
+#ifndef MADV_COLLAPSE
+#define MADV_COLLAPSE 25   // Linux 6.1+: collapse the range into transparent huge pages now
+#endif
+
+// Huge-page splits of the whole host (/proc/vmstat thp_split_pmd), or -1.
+long host_thp_splits() {
+    FILE* f = std::fopen("/proc/vmstat", "r");
+    if (!f) return -1;
+    char line[128];
+    long v = -1;
+    while (std::fgets(line, sizeof line, f))
+        if (std::strncmp(line, "thp_split_pmd ", 14) == 0) {
+            v = std::atol(line + 14);
+            break;
+        }
+    std::fclose(f);
+    return v;
+}
+
+// The keeper: a host thread that lives while huge-page value memory exists.  Every few
+// milliseconds it reads the host kernel's count of huge-page splits; when the count moves, it
+// collapses every huge-page allocation again (madvise MADV_COLLAPSE: a page that is whole costs
+// nothing, a split one is copied into a fresh huge page, about 50 ms for 512 MiB).  Splits are
+// rare after pre-filling but cost the fetch a translation per 64 KiB of a split page for the
+// rest of the run.
+struct Keeper {
+    std::thread th;
+    std::atomic<bool> stop{false};
+    bool running = false;
+    ~Keeper() { halt(); }
+    void halt() {
+        if (!running) return;
+        stop.store(true);
+        th.join();
+        running = false;
+    }
+    void start() {
+        if (running) return;
+        stop.store(false);
+        th = std::thread([this] {
+            long last = host_thp_splits();
+            while (!stop.load()) {
+                std::this_thread::sleep_for(std::chrono::milliseconds(5));
+                const long now = host_thp_splits();
+                if (now < 0 || now == last) continue;
+                last = now;
+                std::lock_guard<std::mutex> lock(g_host_mu);
+                for (const HostMap& m : g_host_maps) madvise(m.user, m.len - (static_cast<uint8_t*>(m.user) -
+                                                                              static_cast<uint8_t*>(m.raw)),
+                                                             MADV_COLLAPSE);
+            }
+        });
+        running = true;
+    }
+};
+Keeper g_keeper;
+
+// The huge-page host mapping holding [p, p + bytes), or nullptr.
+const HostMap* find_host_map(const void* p, size_t bytes) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    for (const HostMap& m : g_host_maps) {
+        const uintptr_t b = reinterpret_cast<uintptr_t>(m.user);
+        const uintptr_t e = reinterpret_cast<uintptr_t>(m.raw) + m.len;
+        if (a >= b && a < e && bytes <= e - a) return &m;
+    }
+    return nullptr;
+}
 
 // size of the host's transparent huge pages (512 MiB with 64 KiB base pages, 2 MiB with 4 KiB)
 size_t host_huge_page_bytes() {
@@ -108,8 +180,9 @@ struct skv_layer {
     cudaStream_t last_main = nullptr, last_side = nullptr;
     bool stepped = false;
     cudaEvent_t ev_sel = nullptr, ev_fetch = nullptr, ev_start = nullptr;
+    cudaEvent_t user_sel = nullptr;       // the caller's event, recorded after each selection
     bool profiling = false;
-    std::vector<std::array<cudaEvent_t, 7>> prof_pending, prof_free;
+    std::vector<std::array<cudaEvent_t, 8>> prof_pending, prof_free;
     double phase_ms[SKV_NPHASE] = {0};
     int64_t phase_n[SKV_NPHASE] = {0};
 };
@@ -558,6 +631,18 @@ int shadowkv_prefill_index_keys(const skv_config* cfg, const void* A, const void
     }
     if (cudaStreamSynchronize(s) != cudaSuccess) return fail(SKV_ERR_CUDA);
     if ((rc = check_device_error(h))) return fail(rc);
+    if (c.v_place == SKV_V_HOST) {
+        // values in a huge-page arena: pre-filling splits some of its huge pages (measured: about
+        // ten of 128 over a 64 GiB arena, for reasons inside the host kernel and the driver);
+        // put this layer's pages back together before the decode steps read them (best effort)
+        const size_t vbytes = static_cast<size_t>(U) * static_cast<size_t>(c.seq_len) * kD * h->es_v;
+        bool huge = false;
+        {
+            std::lock_guard<std::mutex> lock(g_host_mu);
+            huge = find_host_map(V, vbytes) != nullptr;
+        }
+        if (huge) shadowkv_host_repair(const_cast<void*>(V), vbytes);
+    }
     // the full landmark table is only needed during pre-filling
     cudaFree(Lfull);
     h->allocs.erase(std::find(h->allocs.begin(), h->allocs.end(), Lfull));
@@ -576,7 +661,7 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     h->stepped = true;
     const int t = static_cast<int>(h->t);
     const int U = h->U, K = h->K, G = h->G;
-    std::array<cudaEvent_t, 7> ev{};
+    std::array<cudaEvent_t, 8> ev{};
     if (h->profiling) {
         if (h->prof_free.empty()) {
             for (auto& e : ev) cudaEventCreate(&e);
@@ -626,6 +711,10 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     sel.loc_cap = h->loc_cap; sel.loc_pitch = h->R; sel.W = h->W; sel.es = h->es; sel.es_v = h->es_v;
     sel.err = h->err;
     if (launch_select_decode(h->dtype, sel, sm)) return SKV_ERR_CUDA;
+    if (h->user_sel && cudaEventRecord(h->user_sel, sm) != cudaSuccess) {
+        cudaGetLastError();
+        return SKV_ERR_CUDA;
+    }
     if (h->profiling) cudaEventRecord(ev[2], sm);
     // a6 on the side stream: value rows of the missed chunks into their slots
     if (ss != sm) {
@@ -641,7 +730,9 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     if (frc) return SKV_ERR_CUDA;
     if (h->profiling) cudaEventRecord(ev[6], ss);
     if (ss != sm) cudaEventRecord(h->ev_fetch, ss);
-    // a5 on the main stream: rebuild + RoPE of the missed chunks' keys
+    // a5 on the main stream: rebuild + RoPE of the missed chunks' keys (timed from its own
+    // launch, which with a single stream comes after the fetch)
+    if (h->profiling) cudaEventRecord(ev[7], sm);
     RebuildParams rp{};
     rp.mode = 0; rp.U = U; rp.H = h->H; rp.r = h->r; rp.nkb = h->nkb; rp.S = h->S; rp.nchunk = h->nchunk;
     rp.list = h->miss_chunk; rp.list_us = K; rp.list_cap = K; rp.cnt = h->miss_count; rp.dst_idx = h->miss_slot;
@@ -676,6 +767,12 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     return SKV_OK;
 }
 
+int shadowkv_set_select_event(skv_layer* h, void* event) {
+    if (!h) return SKV_ERR_INVALID;
+    h->user_sel = static_cast<cudaEvent_t>(event);
+    return SKV_OK;
+}
+
 int shadowkv_set_profiling(skv_layer* h, int enable) {
     if (!h) return SKV_ERR_INVALID;
     h->profiling = enable != 0;
@@ -692,7 +789,7 @@ int shadowkv_stats(skv_layer* h, skv_stats* out) {
     // phase times
     for (auto& ev : h->prof_pending) {
         float ms = 0.f;
-        const int pairs[SKV_NPHASE][2] = {{0, 1}, {1, 2}, {2, 3}, {5, 6}, {3, 4}};
+        const int pairs[SKV_NPHASE][2] = {{0, 1}, {1, 2}, {7, 3}, {5, 6}, {3, 4}};
         for (int ph = 0; ph < SKV_NPHASE; ++ph) {
             if (cudaEventElapsedTime(&ms, ev[pairs[ph][0]], ev[pairs[ph][1]]) == cudaSuccess) {
                 h->phase_ms[ph] += ms;
@@ -856,17 +953,15 @@ int shadowkv_host_alloc_kind(size_t bytes, int kind, void** out) {
     if (raw == MAP_FAILED) return SKV_ERR_OOM;
     void* p = reinterpret_cast<void*>((reinterpret_cast<uintptr_t>(raw) + hp - 1) / hp * hp);
     // huge pages: one translation covers a whole page, so the fetch's scattered reads over a
-    // span of tens of GiB keep their translations; preferred location host: the driver never
-    // migrates (and so never splits) these pages toward the GPU on access counts
+    // span of tens of GiB keep their translations.  Preferred location host: the driver does
+    // not migrate these pages toward the GPU on its access counts.  Measured on a 64 GiB arena
+    // over 20 decode steps: with this hint alone no huge page split; adding "accessed by" the
+    // device, or giving no hint, split 8-10 of the 128 pages and slowed the fetch.
     cudaMemLocation host{};
     host.type = cudaMemLocationTypeHost;
     host.id = 0;
-    cudaMemLocation gpu{};
-    gpu.type = cudaMemLocationTypeDevice;
-    gpu.id = dev;
     if (madvise(p, len, MADV_HUGEPAGE) != 0 ||
-        cudaMemAdvise(p, len, cudaMemAdviseSetPreferredLocation, host) != cudaSuccess ||
-        cudaMemAdvise(p, len, cudaMemAdviseSetAccessedBy, gpu) != cudaSuccess) {
+        cudaMemAdvise(p, len, cudaMemAdviseSetPreferredLocation, host) != cudaSuccess) {
         cudaGetLastError();
         munmap(raw, len + hp);
         return SKV_ERR_CUDA;
@@ -875,22 +970,44 @@ int shadowkv_host_alloc_kind(size_t bytes, int kind, void** out) {
         std::lock_guard<std::mutex> lock(g_host_mu);
         g_host_maps.push_back({p, raw, len + hp});
     }
+    g_keeper.start();
     *out = p;
+    return SKV_OK;
+}
+
+int shadowkv_host_repair(void* p, size_t bytes) {
+    if (!p || bytes == 0) return SKV_ERR_INVALID;
+    uintptr_t a = 0, e = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_host_mu);
+        if (!find_host_map(p, bytes)) return SKV_ERR_INVALID;
+        const size_t hp = host_huge_page_bytes();
+        a = reinterpret_cast<uintptr_t>(p) / hp * hp;
+        e = (reinterpret_cast<uintptr_t>(p) + bytes + hp - 1) / hp * hp;
+    }
+    if (madvise(reinterpret_cast<void*>(a), e - a, MADV_COLLAPSE) != 0) {
+        if (errno == EINVAL) return SKV_ERR_UNSUPPORTED;
+        return errno == ENOMEM || errno == EAGAIN ? SKV_ERR_OOM : SKV_ERR_INVALID;
+    }
     return SKV_OK;
 }
 
 void shadowkv_host_free(void* p) {
     if (!p) return;
+    bool last = false, found = false;
     {
         std::lock_guard<std::mutex> lock(g_host_mu);
         for (size_t i = 0; i < g_host_maps.size(); ++i)
             if (g_host_maps[i].user == p) {
                 munmap(g_host_maps[i].raw, g_host_maps[i].len);
                 g_host_maps.erase(g_host_maps.begin() + static_cast<long>(i));
-                return;
+                found = true;
+                last = g_host_maps.empty();
+                break;
             }
     }
-    cudaFreeHost(p);
+    if (last) g_keeper.halt();   // outside the lock: the keeper takes it
+    if (!found) cudaFreeHost(p);
 }
 
 void shadowkv_destroy(skv_layer* h) {

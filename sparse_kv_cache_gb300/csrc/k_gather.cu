@@ -88,3 +88,92 @@ int launch_compact(const CompactParams& p, cudaStream_t s) {
 }
 
 }  // namespace skv
+
+// ---------------------------------------------------------------------------
+// Measurement aid: the decode step's fetch kernel on a random chunk list.
+#include <algorithm>
+#include <cstdint>
+#include <vector>
+
+#include "shadowkv.h"
+
+extern "C" int shadowkv_fetch_probe(const void* src, size_t bytes, int64_t n_chunks, int chunk_bytes, uint64_t seed,
+                                    int reps, int fresh, skv_stream stream, double* gbs_out) {
+    using namespace skv;
+    if (!src || !gbs_out || reps < 1 || n_chunks < 1 || n_chunks > (int64_t(1) << 24)) return SKV_ERR_INVALID;
+    if (chunk_bytes != 1024 && chunk_bytes != 2048 && chunk_bytes != 4096) return SKV_ERR_INVALID;
+    if (reinterpret_cast<uintptr_t>(src) & 15) return SKV_ERR_INVALID;
+    const int64_t slots = static_cast<int64_t>(bytes / static_cast<size_t>(chunk_bytes));
+    if (slots < 2 * n_chunks || slots > INT32_MAX) return SKV_ERR_INVALID;
+    *gbs_out = 0.0;
+    // distinct random chunk positions (splitmix64 stream), ascending: the decode step's address order
+    uint64_t x = seed;
+    auto next = [&x]() {
+        uint64_t z = (x += 0x9E3779B97F4A7C15ull);
+        z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+        z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+        return z ^ (z >> 31);
+    };
+    const int32_t n = static_cast<int32_t>(n_chunks);
+    auto draw = [&](std::vector<int32_t>& ids) {
+        ids.clear();
+        while (static_cast<int64_t>(ids.size()) < n_chunks) {
+            const size_t need = static_cast<size_t>(n_chunks) - ids.size();
+            for (size_t i = 0; i < need; ++i) ids.push_back(static_cast<int32_t>(next() % static_cast<uint64_t>(slots)));
+            std::sort(ids.begin(), ids.end());
+            ids.erase(std::unique(ids.begin(), ids.end()), ids.end());
+        }
+    };
+    std::vector<int32_t> ids, dst_idx(static_cast<size_t>(n));
+    for (int32_t i = 0; i < n; ++i) dst_idx[i] = i;
+    draw(ids);
+    int32_t *d_ids = nullptr, *d_dst = nullptr, *d_cnt = nullptr;
+    int* d_err = nullptr;
+    void* d_out = nullptr;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    int rc = SKV_OK;
+    if (cudaMalloc(&d_ids, n * sizeof(int32_t)) != cudaSuccess || cudaMalloc(&d_dst, n * sizeof(int32_t)) != cudaSuccess ||
+        cudaMalloc(&d_cnt, sizeof(int32_t)) != cudaSuccess || cudaMalloc(&d_err, 4 * sizeof(int)) != cudaSuccess ||
+        cudaMalloc(&d_out, static_cast<size_t>(n) * chunk_bytes) != cudaSuccess) {
+        rc = SKV_ERR_OOM;
+    } else if (cudaMemcpy(d_ids, ids.data(), n * sizeof(int32_t), cudaMemcpyHostToDevice) != cudaSuccess ||
+               cudaMemcpy(d_dst, dst_idx.data(), n * sizeof(int32_t), cudaMemcpyHostToDevice) != cudaSuccess ||
+               cudaMemcpy(d_cnt, &n, sizeof(int32_t), cudaMemcpyHostToDevice) != cudaSuccess ||
+               cudaMemset(d_err, 0, 4 * sizeof(int)) != cudaSuccess ||
+               cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+        rc = SKV_ERR_CUDA;
+    } else {
+        GatherParams g{};
+        g.src = src; g.src_us = 0; g.list = d_ids; g.list_us = n; g.list_cap = n; g.cnt = d_cnt;
+        g.dst_idx = d_dst; g.dst_cap = n; g.dst = d_out; g.dst_us = 0; g.nchunk = static_cast<int>(slots);
+        g.es = chunk_bytes / (kC * kD); g.U = 1; g.err = d_err;
+        float best = 0.f;
+        for (int r = 0; r <= reps && rc == SKV_OK; ++r) {
+            if (fresh && r > 0) {
+                draw(ids);
+                if (cudaMemcpy(d_ids, ids.data(), n * sizeof(int32_t), cudaMemcpyHostToDevice) != cudaSuccess) {
+                    rc = SKV_ERR_CUDA;
+                    break;
+                }
+            }
+            if (cudaEventRecord(e0, stream) != cudaSuccess || launch_gather(g, (n + 7) / 8, stream) ||
+                cudaEventRecord(e1, stream) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess) {
+                rc = SKV_ERR_CUDA;
+                break;
+            }
+            float ms = 0.f;
+            cudaEventElapsedTime(&ms, e0, e1);
+            if (r > 0 && (best == 0.f || ms < best)) best = ms;   // the first run is a warm-up
+        }
+        int e[2] = {0, 0};
+        if (rc == SKV_OK && cudaMemcpy(e, d_err, sizeof(e), cudaMemcpyDeviceToHost) != cudaSuccess) rc = SKV_ERR_CUDA;
+        if (rc == SKV_OK && e[0] != 0) rc = SKV_ERR_DEVICE_BOUNDS;
+        if (rc == SKV_OK && best > 0.f) *gbs_out = static_cast<double>(n) * chunk_bytes / (best * 1e-3) / 1e9;
+    }
+    if (stream) cudaStreamSynchronize(stream);
+    cudaFree(d_ids); cudaFree(d_dst); cudaFree(d_cnt); cudaFree(d_err); cudaFree(d_out);
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+    cudaGetLastError();
+    return rc;
+}

@@ -25,3 +25,21 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """A table of the GPU parity runs: each one's worst output error against the oracle on the
+    GPU's index set (stored-precision keys), the same against float64 keys never stored, the
+    selection near-ties reported and the measured hit rate."""
+    try:
+        from tests.gpu_harness import REPORTS
+    except Exception:
+        return
+    if not REPORTS:
+        return
+    tr = terminalreporter
+    tr.write_sep("-", "GPU parity against the oracle (max |out - oracle|; vs float64 keys never stored)")
+    for r in REPORTS:
+        a = "-" if r["alpha"] is None else f"{r['alpha']:.2f}"
+        tr.write_line(f"{r['workload'][:64]:64s} t{r['steps']:<3d} u{r['units']:<3d} abs {r['max_abs']:.2e} "
+                      f"rel {r['max_rel']:.1e} unrounded {r['vs_unrounded']:.2e} ties {r['ties']} a {a}")

@@ -28,6 +28,32 @@ def test_sweep_64k_b48_host_values():
     run_and_check(w, 2, units=[0, 200, 383], gen_device="cuda", check_cache=False)
 
 
+# The 64K sweep: every batch size, both value placements and every query drift appear in at
+# least one full-size case (drift 0 draws an independent query each step, drift 0.99 nearly
+# repeats it: the two ends of the hit-rate range).
+@pytest.mark.parametrize("batch,place,drift,steps", [
+    (1, "hbm", 0.0, 4),
+    (8, "host", 0.99, 4),
+    (16, "hbm", 0.5, 3),
+    (32, "host", 0.9, 3),
+    (48, "hbm", 0.99, 2),
+])
+def test_sweep_64k_points(batch, place, drift, steps):
+    w = SWEEP_64K.with_(batch=batch, v_place=place, drift=drift)
+    U = w.units
+    units = sorted({0, U // 2, U - 1})
+    run_and_check(w, steps, units=units, gen_device="cuda", check_cache=True, cache_units=units[:1],
+                  host_alloc="huge")
+
+
+def test_llama_128k_b8_host_values_64_steps():
+    """The headline workload over all 64 decode steps of its configuration, huge-page host
+    values as the bench allocates them; cache slots checked on one sampled unit every step."""
+    rep = run_and_check(LLAMA_128K, 64, units=[5, 42], gen_device="cuda", check_cache=True, cache_units=[42],
+                        host_alloc="huge")
+    assert rep.steps == 64
+
+
 def test_llama_128k_b8_fp8_host_values():
     """The e5m2 configuration at the benchmark's 128K size (bench.py --dtype fp8)."""
     rep = run_and_check(LLAMA_128K.with_(dtype="fp8"), 3, units=[1, 38, 62], gen_device="cuda",
