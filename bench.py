@@ -522,6 +522,8 @@ def kernel_rooflines(w: Workload, M: int, st2: list, phase_ms: dict, phase_n: di
     ]
     rows = []
     for ph, name, bound, nbytes in spec:
+        if ph == "fetch" and phase_n[ph] == 0:
+            continue   # values in HBM read in place by attention: no fetch kernel
         n = max(1, phase_n[ph])
         us = 1000.0 * phase_ms[ph] / n
         gbs = nbytes / (us * 1e-6) / 1e9 if us > 0 else 0.0
@@ -616,7 +618,7 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
     t_hbm = hbm_step / (peak_hbm * 1e9) * 1e3
     t_link = link_step / (link_peak * 1e9) * 1e3 if link_peak else 0.0
     binding = "link" if t_link > t_hbm else "hbm"
-    dom = by["fetch"] if binding == "link" else max(
+    dom = by["fetch"] if binding == "link" and "fetch" in by else max(
         (k for k in kernels if k["bound"] == "hbm"), key=lambda k: k["avg_launch_us"] * k["launches"])
     traffic = score_traffic_per_launch(w.with_(batch=w.batch // M)) if dom["phase"] == "score" else None
     roofline = {

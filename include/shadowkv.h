@@ -155,7 +155,10 @@ int shadowkv_prefill_index_keys(const skv_config* cfg, const void* A, const void
  *   3. index scan against the previous step's I: hit chunks keep their cache
  *      slot, missed chunks take the freed slots;
  *   4. rebuilds the missed chunks' keys RoPE(A[rows].B[b][h]) into their slots
- *      (main stream) while their values are gathered from V (side stream);
+ *      (main stream) while their values are gathered from V (side stream); with
+ *      values in HBM and bf16 or e5m2 storage nothing is gathered: attention
+ *      reads every cache slot's values in V, and runs on `main` right after the
+ *      rebuild;
  *   5. out = softmax(q.K^T / sqrt(d)).V over the O*C outlier tokens, the K*C
  *      cached tokens and the W + t + 1 local tokens (t = 0-based step).
  *
@@ -233,7 +236,9 @@ int shadowkv_set_profiling(skv_layer* layer, int enable);
 #define SKV_F_K_LOCAL       6   /* [b*H][W + max_new_tokens][d] dtype */
 #define SKV_F_V_LOCAL       7   /* [b*H][W + max_new_tokens][d] dtype */
 #define SKV_F_K_CACHE       8   /* [b*H][K][C][d] dtype, by slot */
-#define SKV_F_V_CACHE       9   /* [b*H][K][C][d] dtype, by slot */
+#define SKV_F_V_CACHE       9   /* [b*H][K][C][d] dtype, by slot (values in HBM, bf16 or e5m2: the
+                                   rows attention reads in V for each slot, gathered by the export;
+                                   dst must be device memory) */
 #define SKV_F_SELECTION    10   /* [b*H][K] int32: current I, ascending chunk ids */
 #define SKV_F_SLOT_OF_SEL  11   /* [b*H][K] int32: cache slot of each entry of I */
 #define SKV_F_MISS_COUNT   12   /* [b*H] int32: misses of the last step */

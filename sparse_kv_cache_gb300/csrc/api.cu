@@ -157,6 +157,8 @@ struct skv_layer {
     int32_t* sel_ids[2] = {nullptr, nullptr};
     int32_t* sel_slot[2] = {nullptr, nullptr};
     int32_t *miss_chunk = nullptr, *miss_slot = nullptr, *miss_count = nullptr;
+    int32_t* slot_chunk = nullptr;        // [U][K] chunk id of each cache slot
+    bool v_direct = false;                // values in HBM read in place by attention (tensor-core path)
     float* logits = nullptr;
     float2* score_part = nullptr;
     float* vbuf = nullptr;
@@ -304,7 +306,13 @@ void step_bytes(const skv_config& c, int64_t t, double misses, double* hbm, doub
         h += es * (2.0 * U * r * d + c.batch * r + U * r);
     }
     double l = misses * C * d * esv;                 // value rows over the host link
-    if (c.v_place == SKV_V_HBM) { h += l; l = 0.0; }
+    if (c.v_place == SKV_V_HBM) {
+        // values in HBM: the fp32 path copies missed rows into the value cache (one more read);
+        // the tensor-core path's attention reads them in V, so no slot is written either
+        if (c.dtype == SKV_F32) h += l;
+        else h -= misses * C * esv * d;
+        l = 0.0;
+    }
     const double nsplit = std::ceil((O * C + K * C + loc) / attn_segment(c.dtype));
     *hbm = h;
     *link = l;
@@ -428,6 +436,9 @@ int shadowkv_prefill_index_keys(const skv_config* cfg, const void* A, const void
     h->es_l = es_l_of(c.dtype);
     h->es_v = es_v_of(c.dtype);
     h->tc = c.dtype != SKV_F32;
+    // with values in HBM the tensor-core attention reads a selected chunk's values where they
+    // live: no copy into a value cache, and the attention follows the rebuild on one stream
+    h->v_direct = h->tc && c.v_place == SKV_V_HBM;
     h->nkb = (h->r + 63) / 64;
     h->newkeys = c.new_keys;
     h->Tpad = (h->Tmax + kC - 1) / kC * kC;
@@ -494,6 +505,7 @@ int shadowkv_prefill_index_keys(const skv_config* cfg, const void* A, const void
         (rc = alloc_t(h, &h->miss_chunk, static_cast<size_t>(U) * K)) ||
         (rc = alloc_t(h, &h->miss_slot, static_cast<size_t>(U) * K)) ||
         (rc = alloc_t(h, &h->miss_count, static_cast<size_t>(U))) ||
+        (rc = alloc_t(h, &h->slot_chunk, static_cast<size_t>(U) * K)) ||
         (rc = alloc_t(h, &h->logits, U * nc * G)) ||
         (rc = alloc_t(h, &h->score_part, static_cast<size_t>(U) * h->score_nru * h->score_nparts * G)) ||
         (rc = alloc_t(h, &h->sched, 1)) ||
@@ -707,6 +719,7 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     sel.prev_ids = h->sel_ids[t & 1]; sel.prev_slot = h->sel_slot[t & 1];
     sel.cur_ids = h->sel_ids[(t + 1) & 1]; sel.cur_slot = h->sel_slot[(t + 1) & 1];
     sel.miss_chunk = h->miss_chunk; sel.miss_slot = h->miss_slot; sel.miss_count = h->miss_count;
+    sel.slot_chunk = h->slot_chunk;
     sel.hits_step = h->hits_step; sel.k_new = h->newkeys == SKV_NEWKEYS_LOWRANK ? nullptr : k_new; sel.v_new = v_new; sel.k_loc = h->Kloc; sel.v_loc = h->Vloc;
     sel.loc_cap = h->loc_cap; sel.loc_pitch = h->R; sel.W = h->W; sel.es = h->es; sel.es_v = h->es_v;
     sel.err = h->err;
@@ -716,20 +729,25 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
         return SKV_ERR_CUDA;
     }
     if (h->profiling) cudaEventRecord(ev[2], sm);
-    // a6 on the side stream: value rows of the missed chunks into their slots
-    if (ss != sm) {
-        cudaEventRecord(h->ev_sel, sm);
-        cudaStreamWaitEvent(ss, h->ev_sel, 0);
+    // a6 on the side stream: value rows of the missed chunks into their slots.  With values in
+    // HBM on the tensor-core path there is nothing to move: attention reads them in V.
+    // side_pending: the side stream holds work attention must wait for
+    const bool side_pending = ss != sm && (!h->v_direct || h->newkeys == SKV_NEWKEYS_LOWRANK);
+    if (!h->v_direct) {
+        if (ss != sm) {
+            cudaEventRecord(h->ev_sel, sm);
+            cudaStreamWaitEvent(ss, h->ev_sel, 0);
+        }
+        if (h->profiling) cudaEventRecord(ev[5], ss);
+        GatherParams g{};
+        g.src = h->Vd; g.src_us = h->S * kD; g.list = h->miss_chunk; g.list_us = K; g.list_cap = K;
+        g.cnt = h->miss_count; g.dst_idx = h->miss_slot; g.dst_cap = K; g.dst = h->Vc;
+        g.dst_us = h->R * kD; g.nchunk = h->nchunk; g.es = h->es_v; g.U = U; g.err = h->err;
+        const int frc = launch_gather(g, (K + 7) / 8, ss);
+        if (frc) return SKV_ERR_CUDA;
+        if (h->profiling) cudaEventRecord(ev[6], ss);
     }
-    if (h->profiling) cudaEventRecord(ev[5], ss);
-    GatherParams g{};
-    g.src = h->Vd; g.src_us = h->S * kD; g.list = h->miss_chunk; g.list_us = K; g.list_cap = K;
-    g.cnt = h->miss_count; g.dst_idx = h->miss_slot; g.dst_cap = K; g.dst = h->Vc;
-    g.dst_us = h->R * kD; g.nchunk = h->nchunk; g.es = h->es_v; g.U = U; g.err = h->err;
-    const int frc = launch_gather(g, (K + 7) / 8, ss);
-    if (frc) return SKV_ERR_CUDA;
-    if (h->profiling) cudaEventRecord(ev[6], ss);
-    if (ss != sm) cudaEventRecord(h->ev_fetch, ss);
+    if (side_pending) cudaEventRecord(h->ev_fetch, ss);
     // a5 on the main stream: rebuild + RoPE of the missed chunks' keys (timed from its own
     // launch, which with a single stream comes after the fetch)
     if (h->profiling) cudaEventRecord(ev[7], sm);
@@ -742,7 +760,7 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     const int rc = h->tc ? launch_rebuild_tc(&h->tmA, &h->tmB, rp, gx, sm) : launch_rebuild_f32(rp, gx, sm);
     if (rc) return SKV_ERR_CUDA;
     if (h->profiling) cudaEventRecord(ev[3], sm);
-    if (ss != sm) cudaStreamWaitEvent(sm, h->ev_fetch, 0);
+    if (side_pending) cudaStreamWaitEvent(sm, h->ev_fetch, 0);
     // a7: attention over outliers + cache + local, split-K with an in-kernel merge
     AttnParams ap{};
     ap.q = q; ap.k_out = h->Kout; ap.v_out = h->Vout; ap.n_out = h->O * kC;
@@ -754,11 +772,16 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     ap.nsplit = (ap.n_out + ap.n_cache + ap.n_loc + seg - 1) / seg;
     ap.scale = sp.scale; ap.G = G; ap.U = U; ap.err = h->err;
     ap.v_es = h->es_v;
+    if (h->v_direct) {
+        ap.v_src = h->Vd; ap.v_src_us = h->S * kD; ap.slot_chunk = h->slot_chunk; ap.nchunk = h->nchunk;
+        ap.pdl = side_pending ? 0 : 1;   // a programmatic dependent of the rebuild, on one stream
+    }
     const int na = h->tc ? launch_attn_tc(&h->tmKall, ap, h->sm_count, sm) : (launch_attn(h->dtype, ap, sm) ? -1 : 1);
     if (na < 0) return SKV_ERR_CUDA;
-    // score, select, fetch, rebuild, attention (+ its merge); the e5m2 query split; ShadowKV+'s
-    // projection and new key
-    h->launches += 4 + na + (h->dtype == SKV_FP8 ? 1 : 0) + (h->newkeys == SKV_NEWKEYS_LOWRANK ? 2 : 0);
+    // score, select, fetch (not with values read in place), rebuild, attention (+ its merge); the
+    // e5m2 query split; ShadowKV+'s projection and new key
+    h->launches += (h->v_direct ? 3 : 4) + na + (h->dtype == SKV_FP8 ? 1 : 0) +
+                   (h->newkeys == SKV_NEWKEYS_LOWRANK ? 2 : 0);
     if (h->profiling) {
         cudaEventRecord(ev[4], sm);
         h->prof_pending.push_back(ev);
@@ -890,6 +913,17 @@ int shadowkv_export(skv_layer* h, int field, void* dst, size_t bytes, skv_stream
         case SKV_F_A_NEW: src = h->Anew; break;
     }
     if (need == 0) return SKV_OK;
+    if (field == SKV_F_V_CACHE && h->v_direct) {
+        // values read in place: the rows attention reads for each slot, gathered from V by the
+        // slot's chunk
+        if (!is_device_ptr(dst)) return SKV_ERR_INVALID;
+        GatherParams g{};
+        g.src = h->Vd; g.src_us = h->S * kD; g.list = h->slot_chunk; g.list_us = h->K; g.list_cap = h->K;
+        g.cnt = nullptr; g.count_const = h->K; g.dst_idx = nullptr; g.dst_cap = h->K; g.dst = dst;
+        g.dst_us = static_cast<int64_t>(h->K) * kC * kD; g.nchunk = h->nchunk; g.es = h->es_v; g.U = h->U;
+        g.err = h->err;
+        return launch_gather(g, (h->K + 7) / 8, stream) ? SKV_ERR_CUDA : SKV_OK;
+    }
     // fields inside the per-unit key/value blocks: [U][rows][d] out of rows of pitch R
     int64_t rows = 0;
     switch (field) {

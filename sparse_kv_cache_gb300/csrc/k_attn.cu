@@ -479,6 +479,9 @@ __global__ void __launch_bounds__((kAWarps + 2) * 32, 1) k_attn_tc(const __grid_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
+    // launched as a programmatic dependent of the key rebuild (values in HBM): the prologue
+    // above overlapped its tail; everything below reads what the earlier kernels wrote
+    pdl_wait();
     // the merge kernel that follows may be scheduled beside this grid now; it waits for the
     // whole grid before it reads a partial
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -502,17 +505,45 @@ __global__ void __launch_bounds__((kAWarps + 2) * 32, 1) k_attn_tc(const __grid_
             uint8_t* sK = smb + st * kAStage;
             uint8_t* sQ = sK + kAKBytes;
             uint8_t* sV = sQ + kAQBytes;
+            // cache rows of the segment whose values are read where they live (values in HBM):
+            // lane i copies the rows of the segment's i-th cache slot from its chunk in V
+            const int c0 = p.v_src ? max(seg0, p.n_out) : 0;
+            const int c1 = p.v_src ? min(seg0 + nseg, p.n_out + p.n_cache) : 0;
+            const int nvc = c1 > c0 ? (c1 - c0) / kC : 0;
+            int vch = 0;
+            if (lane < nvc) {
+                vch = p.slot_chunk[static_cast<int64_t>(ua) * (p.n_cache / kC) + (c0 - p.n_out) / kC + lane];
+                if (vch < 0 || vch >= p.nchunk) {
+                    set_err(p.err, DEV_ERR_BOUNDS, 625);
+                    vch = 0;   // read a valid chunk: the expected bytes still arrive
+                }
+            }
             if (lane == 0) {
                 // the unit's block holds the segment's rows contiguously: two 128-row key boxes
                 // (rows past the unit's tokens are read but scored -inf; past the last block the
-                // copy fills zeros) and one bulk copy of the value rows
+                // copy fills zeros) and one bulk copy of the value rows (around the cache rows
+                // when those are read from V)
                 const int row = static_cast<int>(static_cast<int64_t>(ua) * p.unit_rows + seg0);
                 mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(kAKBytes + nseg * kD * VB));
                 tma_load_2d_hint(sK, &tmK, 0, row, &full[st], pol);
                 tma_load_2d_hint(sK + 16384, &tmK, 64, row, &full[st], pol);
-                bulk_g2s_hint(sV, static_cast<const uint8_t*>(p.v_out) + (static_cast<int64_t>(ua) * p.unit_rows + seg0) * kD * VB,
-                              static_cast<uint32_t>(nseg) * kD * VB, &full[st], pol);
+                const uint8_t* vb = static_cast<const uint8_t*>(p.v_out) + (static_cast<int64_t>(ua) * p.unit_rows + seg0) * kD * VB;
+                if (nvc > 0) {
+                    if (c0 > seg0)
+                        bulk_g2s_hint(sV, vb, static_cast<uint32_t>(c0 - seg0) * kD * VB, &full[st], pol);
+                    if (seg0 + nseg > c1)
+                        bulk_g2s_hint(sV + (c1 - seg0) * kD * VB, vb + static_cast<int64_t>(c1 - seg0) * kD * VB,
+                                      static_cast<uint32_t>(seg0 + nseg - c1) * kD * VB, &full[st], pol);
+                } else {
+                    bulk_g2s_hint(sV, vb, static_cast<uint32_t>(nseg) * kD * VB, &full[st], pol);
+                }
             }
+            __syncwarp();
+            if (lane < nvc)
+                bulk_g2s_hint(sV + (c0 - seg0 + lane * kC) * kD * VB,
+                              static_cast<const uint8_t*>(p.v_src) + (static_cast<int64_t>(ua) * p.v_src_us +
+                                                                      static_cast<int64_t>(vch) * kC * kD) * VB,
+                              static_cast<uint32_t>(kC * kD * VB), &full[st], pol);
             // the unit's query rows g < G (the MMA's other columns are never read), written while
             // the copies are in flight; the second arrival publishes them
 #pragma unroll
@@ -808,9 +839,17 @@ static int launch_tc(const CUtensorMap* tmK, const AttnParams& p, int nsm, cudaS
     if (ncta <= 0) return -1;
     if (F * (ncta + 1) > INT32_MAX || static_cast<int64_t>(p.U) * p.unit_rows > INT32_MAX) return -1;   // 32-bit indexing
     const size_t smem = static_cast<size_t>(AStages<G>::value) * kAStage + static_cast<size_t>(4) * G * kD * 4 + 1024;
+    if (p.v_src && (!p.slot_chunk || p.n_cache % kC || p.nchunk <= 0)) return -1;
     cudaFuncSetAttribute(k_attn_tc<G, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    k_attn_tc<G, VB><<<ncta, (kAWarps + 2) * 32, smem, s>>>(*tmK, p);
-    if (cudaGetLastError() != cudaSuccess) return -1;
+    if (p.pdl) {
+        if (launch_pdl(k_attn_tc<G, VB>, dim3(ncta), dim3((kAWarps + 2) * 32), smem, s, *tmK, p) != cudaSuccess) {
+            cudaGetLastError();
+            return -1;
+        }
+    } else {
+        k_attn_tc<G, VB><<<ncta, (kAWarps + 2) * 32, smem, s>>>(*tmK, p);
+        if (cudaGetLastError() != cudaSuccess) return -1;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.U);
     cfg.blockDim = dim3(kD);

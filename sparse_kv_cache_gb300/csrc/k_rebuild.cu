@@ -210,6 +210,9 @@ __global__ void __launch_bounds__(128, 1) k_rebuild_tc(const __grid_constant__ C
     const int u = blockIdx.x, tile = blockIdx.y, tid = threadIdx.x, warp = tid >> 5;
     // launched as a programmatic dependent of the selection: the list is its output
     pdl_wait();
+    // the attention that follows (values in HBM) may be scheduled as this grid's CTAs finish; it
+    // waits for the whole grid before it reads a key
+    pdl_trigger();
     // the list entries are read in the same round trip as the count (in bounds up to list_cap)
     int ch_raw = 0, dst_raw = 0;
     const int first_idx = tile * kTileChunks;

@@ -766,6 +766,7 @@ __device__ __forceinline__ void select_decode(const SelectParams& p) {
         }
         cids[i] = sSel[i];
         cslot[i] = slot;
+        if (p.slot_chunk) p.slot_chunk[static_cast<int64_t>(u) * K + slot] = sSel[i];
         if (p.sel_out_user) p.sel_out_user[static_cast<int64_t>(u) * K + i] = sSel[i];
     }
     if (tid == 0) {

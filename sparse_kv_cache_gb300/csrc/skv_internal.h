@@ -75,6 +75,7 @@ struct SelectParams {
     int32_t* prev_ids; int32_t* prev_slot;   // [U][K]
     int32_t* cur_ids; int32_t* cur_slot;     // [U][K]
     int32_t* miss_chunk; int32_t* miss_slot; int32_t* miss_count;  // [U][K], [U]
+    int32_t* slot_chunk;  // [U][K] chunk id held by each cache slot, or NULL
     int32_t* hits_step;   // [max_new_tokens]
     // append of the new token
     const void* k_new; const void* v_new; void* k_loc; void* v_loc;
@@ -154,6 +155,11 @@ struct AttnParams {
     // every region start at base + u * unit_rows); 0: each region is packed [U][its rows][d]
     int64_t unit_rows;
     int v_es;                      // bytes of a value element: 2 (bf16) or 1 (e5m2; tensor-core form only)
+    // values of the cache rows read where they live (values in HBM; tensor-core form only): the
+    // chunk of cache slot s of unit u is slot_chunk[u * n_cache / 8 + s], its rows start at
+    // v_src + (u * v_src_us + chunk * 8) * 128 elements; NULL: the cache rows' values come from v_c
+    const void* v_src; int64_t v_src_us; const int32_t* slot_chunk; int nchunk;
+    int pdl;                       // launched as a programmatic dependent of the previous kernel
     void* out;                     // [U*G][d]
     float* part;                   // [U][nsplit][G][d + 4]
     int* counter;                  // [U]

@@ -136,3 +136,21 @@ def test_step_bytes_match_the_byte_model_by_hand(lib):
     m = lib.model(cfg, 0.6, 32, 8000.0, 400.0)
     per_step = 32 * (m["hbm_bytes_per_step"])
     assert 12.0e9 < per_step < 13.2e9
+
+
+def test_step_bytes_by_value_placement(lib):
+    # the missed chunks' values: over the link with host values; with values in HBM the
+    # tensor-core path's attention reads them where they live (no slot write, no extra read),
+    # while the fp32 path copies them into the value cache (one more read)
+    w = LLAMA_128K
+    U, C, d, K = w.units, w.chunk, w.head_dim, w.n_select
+    misses = 0.4 * K * U
+    host = lib.model(lib.make_config(w), 0.6, 32, 8000.0, 400.0)
+    hbm = lib.model(lib.make_config(w.with_(v_place="hbm")), 0.6, 32, 8000.0, 400.0)
+    assert host["link_bytes_per_step"] == pytest.approx(misses * C * d * 2)
+    assert hbm["link_bytes_per_step"] == 0
+    assert hbm["hbm_bytes_per_step"] == pytest.approx(host["hbm_bytes_per_step"] - misses * C * d * 2)
+    f32 = w.with_(dtype="f32")
+    h32 = lib.model(lib.make_config(f32), 0.6, 32, 8000.0, 400.0)
+    d32 = lib.model(lib.make_config(f32.with_(v_place="hbm")), 0.6, 32, 8000.0, 400.0)
+    assert d32["hbm_bytes_per_step"] == pytest.approx(h32["hbm_bytes_per_step"] + h32["link_bytes_per_step"])
