@@ -41,6 +41,7 @@ METRIC = "sparse decode-attention tokens/s and HBM GB/s (% of 8 TB/s) at 128K, 1
 UNIT = "tokens/s"
 HBM_NOMINAL_GBS = 8000.0
 EQBW_TOLERANCE = 0.25   # measured step time within +-25 % of the equivalent-bandwidth prediction
+HUGE_SPLIT_LIMIT = 0.25  # more huge-page splits than this share of the arena's pages during setup: page-locked
 
 
 def parse(argv=None):
@@ -74,9 +75,9 @@ def parse(argv=None):
     ap.add_argument("--pipeline", action="store_true",
                     help="with --microbatches M >= 2: stagger the micro-batches, each one's scoring waits for "
                          "the previous one's selection, so one's value fetch overlaps the next one's scoring")
-    ap.add_argument("--host-mem", default="huge", choices=["pinned", "huge"],
+    ap.add_argument("--host-mem", default="pinned", choices=["pinned", "huge"],
                     help="host values: page-locked memory, or transparent huge pages read through the host "
-                         "page tables")
+                         "page tables (faster while the host kernel keeps the pages whole)")
     ap.add_argument("--single-stream", action="store_true",
                     help="run the value fetch on the main stream too (fetch, then rebuild)")
     return ap.parse_args(argv)
@@ -558,12 +559,28 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
     for _ in range(W):
         R.step()
     torch.cuda.synchronize()
-    repair = None
+    repair, fallback = None, None
     if R.arena is not None and R.arena.kind == "huge":
         # huge pages split during the warm-up steps are put back together before timing
         t_r = time.time()
         rc = R.arena.repair()
         repair = {"status": rc, "seconds": time.time() - t_r}
+        splits = thp_counters().get("thp_split_pmd", 0) - thp0.get("thp_split_pmd", 0)
+        pages = R.arena.nbytes / (512 << 20)
+        if splits > HUGE_SPLIT_LIMIT * pages:
+            # the host kernel kept splitting the arena's huge pages while it was filled and the
+            # layers pre-filled (measured once: 86 of 128): measure with page-locked values instead
+            import copy
+            fallback = {"from": "huge", "to": "pinned", "splits_during_setup": splits,
+                        "huge_pages": pages, "limit_fraction": HUGE_SPLIT_LIMIT}
+            R.close()
+            del R
+            args = copy.copy(args)
+            args.host_mem = "pinned"
+            R = Run(args, w, dev, total_steps, ws)
+            for _ in range(W):
+                R.step()
+            torch.cuda.synchronize()
     R.reset_stats()
     R.thp_trace["after_warmup_and_repair"] = thp_counters()
 
@@ -711,6 +728,7 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
         "host_thp_counters_delta": {k: thp1.get(k, 0) - thp0.get(k, 0) for k in thp1},
         "host_thp_trace": thp_trace,
         "host_repair_after_warmup": repair,
+        "host_mem_fallback": fallback,
     }
     if dev_err:
         line["device_error"] = dev_err[0]

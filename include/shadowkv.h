@@ -312,10 +312,11 @@ int shadowkv_host_alloc_kind(size_t bytes, int kind, void** out);
  * together (madvise MADV_COLLAPSE, Linux 6.1+; a page that is whole costs nothing).  Measured
  * on a 64 GiB arena: about ten of its 128 pages split while the layers were pre-filled, and a
  * split page costs the fetch a translation per 64 KiB instead of per 512 MiB.
- * shadowkv_prefill_index repairs the layer's own values before it returns, and while any
- * SKV_HOST_HUGE allocation exists a library thread watches the host's split count
- * (/proc/vmstat thp_split_pmd, every 5 ms) and repairs every such allocation when it moves.
- * A caller may also repair a range itself, e.g. after its warm-up.  Synchronous.
+ * shadowkv_prefill_index repairs the layer's own values before it returns.  From the first
+ * decode step that reads such memory until the last SKV_HOST_HUGE allocation is freed, a
+ * library thread watches the host's split count (/proc/vmstat thp_split_pmd, every 5 ms) and
+ * repairs every such allocation when it moves, resting 50 ms after each repair.  A caller may
+ * also repair a range itself, e.g. after its warm-up.  Synchronous.
  * SKV_ERR_INVALID if the range is not inside such an allocation, SKV_ERR_UNSUPPORTED if the
  * host kernel lacks the call, SKV_ERR_OOM if no huge page could be had.
  */

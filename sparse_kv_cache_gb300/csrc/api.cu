@@ -66,24 +66,30 @@ long host_thp_splits() {
     return v;
 }
 
-// The keeper: a host thread that lives while huge-page value memory exists.  Every few
-// milliseconds it reads the host kernel's count of huge-page splits; when the count moves, it
-// collapses every huge-page allocation again (madvise MADV_COLLAPSE: a page that is whole costs
-// nothing, a split one is copied into a fresh huge page, about 50 ms for 512 MiB).  Splits are
-// rare after pre-filling but cost the fetch a translation per 64 KiB of a split page for the
-// rest of the run.
+// The keeper: a host thread that runs from the first decode step that reads huge-page values
+// until the last such allocation is freed.  Every few milliseconds it reads the host kernel's
+// count of huge-page splits; when the count moves, it collapses every huge-page allocation
+// again (madvise MADV_COLLAPSE: a page that is whole costs nothing, a split one is copied into a
+// fresh huge page, about 50 ms for 512 MiB), and then rests at least 50 ms.  A split page costs
+// the fetch a translation per 64 KiB for the rest of the run.  It does not run while memory is
+// filled and layers are pre-filled: a collapse needs a free huge page, the compaction that finds
+// one can split other pages, and while pages are still being faulted in that feeds on itself
+// (measured once: 86 splits and 104 collapses in one run).  Pre-filling repairs its own layer.
 struct Keeper {
     std::thread th;
     std::atomic<bool> stop{false};
     bool running = false;
+    std::mutex mu;   // start and halt; taken after g_host_mu when both are held
     ~Keeper() { halt(); }
     void halt() {
+        std::lock_guard<std::mutex> lock(mu);
         if (!running) return;
         stop.store(true);
         th.join();
         running = false;
     }
     void start() {
+        std::lock_guard<std::mutex> lock(mu);
         if (running) return;
         stop.store(false);
         th = std::thread([this] {
@@ -92,11 +98,14 @@ struct Keeper {
                 std::this_thread::sleep_for(std::chrono::milliseconds(5));
                 const long now = host_thp_splits();
                 if (now < 0 || now == last) continue;
-                last = now;
-                std::lock_guard<std::mutex> lock(g_host_mu);
-                for (const HostMap& m : g_host_maps) madvise(m.user, m.len - (static_cast<uint8_t*>(m.user) -
-                                                                              static_cast<uint8_t*>(m.raw)),
-                                                             MADV_COLLAPSE);
+                {
+                    std::lock_guard<std::mutex> lock(g_host_mu);
+                    for (const HostMap& m : g_host_maps)
+                        madvise(m.user, m.len - (static_cast<uint8_t*>(m.user) - static_cast<uint8_t*>(m.raw)),
+                                MADV_COLLAPSE);
+                }
+                last = host_thp_splits();   // splits the collapses themselves caused are not chased
+                for (int i = 0; i < 10 && !stop.load(); ++i) std::this_thread::sleep_for(std::chrono::milliseconds(5));
             }
         });
         running = true;
@@ -159,6 +168,7 @@ struct skv_layer {
     int32_t *miss_chunk = nullptr, *miss_slot = nullptr, *miss_count = nullptr;
     int32_t* slot_chunk = nullptr;        // [U][K] chunk id of each cache slot
     bool v_direct = false;                // values in HBM read in place by attention (tensor-core path)
+    bool v_huge = false;                  // values in a huge-page host allocation
     float* logits = nullptr;
     float2* score_part = nullptr;
     float* vbuf = nullptr;
@@ -654,6 +664,7 @@ int shadowkv_prefill_index_keys(const skv_config* cfg, const void* A, const void
             huge = find_host_map(V, vbytes) != nullptr;
         }
         if (huge) shadowkv_host_repair(const_cast<void*>(V), vbytes);
+        h->v_huge = huge;
     }
     // the full landmark table is only needed during pre-filling
     cudaFree(Lfull);
@@ -666,6 +677,10 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
                          int32_t* sel_out, skv_stream main, skv_stream side) {
     if (!h || !q || !k_new || !v_new || !out) return SKV_ERR_INVALID;
     if (h->t >= h->Tmax) return SKV_ERR_STEP_LIMIT;
+    if (h->v_huge && h->t == 0) {
+        std::lock_guard<std::mutex> lock(g_host_mu);
+        if (!g_host_maps.empty()) g_keeper.start();
+    }
     cudaStream_t sm = main;
     cudaStream_t ss = (side == nullptr || side == main) ? main : side;
     h->last_main = sm;
@@ -1004,7 +1019,6 @@ int shadowkv_host_alloc_kind(size_t bytes, int kind, void** out) {
         std::lock_guard<std::mutex> lock(g_host_mu);
         g_host_maps.push_back({p, raw, len + hp});
     }
-    g_keeper.start();
     *out = p;
     return SKV_OK;
 }

@@ -22,7 +22,7 @@ def test_default_workload_is_the_128k_headline():
     args = _args()
     w = bench.workload_from(args)
     assert w == LLAMA_128K
-    assert args.host_mem == "huge" and args.microbatches == 1
+    assert args.host_mem == "pinned" and args.microbatches == 1
     assert (w.seq_len, w.batch, w.layers, w.v_place, w.dtype, w.new_keys) == (131072, 8, 32, "host", "bf16", "exact")
 
 
