@@ -294,12 +294,16 @@ int shadowkv_host_alloc(size_t bytes, void** out);
  *                    own page tables (Grace with NVLink-C2C; SKV_ERR_UNSUPPORTED elsewhere).
  *                    The mapping is aligned to the huge-page size and advised for huge pages;
  *                    the CUDA driver is told that its preferred location is the host, so it
- *                    does not migrate (and split) the pages on the GPU's access counts.  Pages come into being when first written
- *                    (fill it before the first shadowkv_prefill_index that reads it).  One
- *                    translation then covers a whole huge page, and the value fetch's
- *                    scattered 2 KB reads over tens of GiB keep their translations: measured
- *                    for 32 x 2 GiB of values, about 170 GB/s against 125 GB/s from
- *                    page-locked memory (link copy peak about 210 GB/s).
+ *                    does not migrate the pages on the GPU's access counts.  Pages come into
+ *                    being when first written (fill it before the first
+ *                    shadowkv_prefill_index that reads it).  While its pages are whole, one
+ *                    translation covers 512 MiB and the value fetch's scattered 2 KB reads
+ *                    run at about 170 GB/s against 125 GB/s from page-locked memory (32 x
+ *                    2 GiB of values; link copy peak about 210 GB/s).  But the host kernel
+ *                    splits some of them -- measured: a few of 128 pages of a 64 GiB arena on
+ *                    most runs, 40-86 on the first run on a freshly booted host -- and a split
+ *                    page is read with a translation per 64 KiB; see shadowkv_host_repair.
+ *                    SKV_HOST_PINNED is the steady choice.
  * SKV_ERR_INVALID for bytes == 0, out == NULL or an unknown kind; SKV_ERR_OOM if the memory
  * cannot be had.  shadowkv_host_free releases either kind.
  */

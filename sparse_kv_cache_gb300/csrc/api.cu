@@ -43,7 +43,12 @@ int fault_oom_at() {
 }
 
 // huge-page host memory handed out by shadowkv_host_alloc_kind: (user pointer, mapping)
-struct HostMap { void* user; void* raw; size_t len; };
+struct HostMap {
+    void* user;       // the caller's pointer, aligned to the huge-page size
+    size_t user_len;  // the caller's bytes, rounded up to whole huge pages
+    void* raw;        // the whole mapping (with the alignment slack)
+    size_t len;
+};
 std::mutex g_host_mu;
 std::vector<HostMap> g_host_maps;
 
@@ -100,9 +105,7 @@ struct Keeper {
                 if (now < 0 || now == last) continue;
                 {
                     std::lock_guard<std::mutex> lock(g_host_mu);
-                    for (const HostMap& m : g_host_maps)
-                        madvise(m.user, m.len - (static_cast<uint8_t*>(m.user) - static_cast<uint8_t*>(m.raw)),
-                                MADV_COLLAPSE);
+                    for (const HostMap& m : g_host_maps) madvise(m.user, m.user_len, MADV_COLLAPSE);
                 }
                 last = host_thp_splits();   // splits the collapses themselves caused are not chased
                 for (int i = 0; i < 10 && !stop.load(); ++i) std::this_thread::sleep_for(std::chrono::milliseconds(5));
@@ -118,7 +121,7 @@ const HostMap* find_host_map(const void* p, size_t bytes) {
     const uintptr_t a = reinterpret_cast<uintptr_t>(p);
     for (const HostMap& m : g_host_maps) {
         const uintptr_t b = reinterpret_cast<uintptr_t>(m.user);
-        const uintptr_t e = reinterpret_cast<uintptr_t>(m.raw) + m.len;
+        const uintptr_t e = b + m.user_len;
         if (a >= b && a < e && bytes <= e - a) return &m;
     }
     return nullptr;
@@ -1017,7 +1020,7 @@ int shadowkv_host_alloc_kind(size_t bytes, int kind, void** out) {
     }
     {
         std::lock_guard<std::mutex> lock(g_host_mu);
-        g_host_maps.push_back({p, raw, len + hp});
+        g_host_maps.push_back({p, len, raw, len + hp});
     }
     *out = p;
     return SKV_OK;
