@@ -163,6 +163,12 @@ def thp_counters() -> dict:
     return out
 
 
+def huge_storm(splits: int, pages: float) -> bool:
+    """A huge-page arena whose setup split more than HUGE_SPLIT_LIMIT of its pages: measured, the
+    host kernel then keeps splitting, and the bench measures with page-locked values instead."""
+    return splits > HUGE_SPLIT_LIMIT * pages
+
+
 def mem_available_gb() -> float:
     try:
         for line in open("/proc/meminfo"):
@@ -567,7 +573,7 @@ def run_ours(args, w: Workload, ws: int, rank: int, local: int):
         repair = {"status": rc, "seconds": time.time() - t_r}
         splits = thp_counters().get("thp_split_pmd", 0) - thp0.get("thp_split_pmd", 0)
         pages = R.arena.nbytes / (512 << 20)
-        if splits > HUGE_SPLIT_LIMIT * pages:
+        if huge_storm(splits, pages):
             # the host kernel kept splitting the arena's huge pages while it was filled and the
             # layers pre-filled (measured once: 86 of 128): measure with page-locked values instead
             import copy

@@ -100,3 +100,10 @@ def test_kernel_rooflines_use_the_byte_model():
     assert abs(rows["fetch"]["achieved_gbs"] - 100 * U * 8 * 128 * 2 / 1e-4 / 1e9) < 1e-6
     hbm = {r["phase"]: r for r in bench.kernel_rooflines(w.with_(v_place="hbm"), 1, st2, ph, n, 40, 6800.0, None)}
     assert hbm["fetch"]["bound"] == "hbm" and hbm["fetch"]["bytes_per_launch"] == 2 * rows["fetch"]["bytes_per_launch"]
+
+
+def test_huge_page_storm_threshold():
+    # 128 huge pages of a 64 GiB arena: a handful of splits is repaired in place, dozens mean a
+    # storm and the bench falls back to page-locked values
+    assert not bench.huge_storm(0, 128) and not bench.huge_storm(14, 128)
+    assert not bench.huge_storm(32, 128) and bench.huge_storm(33, 128) and bench.huge_storm(86, 128)
