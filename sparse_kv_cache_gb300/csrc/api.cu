@@ -766,6 +766,10 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
         if (h->profiling) cudaEventRecord(ev[6], ss);
     }
     if (side_pending) cudaEventRecord(h->ev_fetch, ss);
+    // values read in place and only ShadowKV+'s small new-key work on the side stream: wait for
+    // it before the rebuild, so that the attention still follows the rebuild directly
+    const bool wait_early = side_pending && h->v_direct;
+    if (wait_early) cudaStreamWaitEvent(sm, h->ev_fetch, 0);
     // a5 on the main stream: rebuild + RoPE of the missed chunks' keys (timed from its own
     // launch, which with a single stream comes after the fetch)
     if (h->profiling) cudaEventRecord(ev[7], sm);
@@ -778,7 +782,7 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     const int rc = h->tc ? launch_rebuild_tc(&h->tmA, &h->tmB, rp, gx, sm) : launch_rebuild_f32(rp, gx, sm);
     if (rc) return SKV_ERR_CUDA;
     if (h->profiling) cudaEventRecord(ev[3], sm);
-    if (side_pending) cudaStreamWaitEvent(sm, h->ev_fetch, 0);
+    if (side_pending && !wait_early) cudaStreamWaitEvent(sm, h->ev_fetch, 0);
     // a7: attention over outliers + cache + local, split-K with an in-kernel merge
     AttnParams ap{};
     ap.q = q; ap.k_out = h->Kout; ap.v_out = h->Vout; ap.n_out = h->O * kC;
@@ -792,7 +796,7 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     ap.v_es = h->es_v;
     if (h->v_direct) {
         ap.v_src = h->Vd; ap.v_src_us = h->S * kD; ap.slot_chunk = h->slot_chunk; ap.nchunk = h->nchunk;
-        ap.pdl = side_pending ? 0 : 1;   // a programmatic dependent of the rebuild, on one stream
+        ap.pdl = 1;   // a programmatic dependent of the rebuild, on one stream
     }
     const int na = h->tc ? launch_attn_tc(&h->tmKall, ap, h->sm_count, sm) : (launch_attn(h->dtype, ap, sm) ? -1 : 1);
     if (na < 0) return SKV_ERR_CUDA;
