@@ -70,3 +70,16 @@ def test_llama_128k_b8_lowrank_new_keys():
 def test_llama_32k_b4_exact_keys():
     """Pre-filling from exact keys at the 32K b4 size."""
     run_and_check(LLAMA_32K, 3, units=[0, 17, 31], gen_device="cuda", check_cache=True, exact_keys=True)
+
+
+def test_llama_1m_b1_hbm_values():
+    """1M context with values in HBM: the attention reads its 2048 cache slots' values in V
+    through the selection's slot -> chunk table, and the selection runs on a cluster."""
+    run_and_check(LLAMA_1M.with_(v_place="hbm"), 2, units=[3], gen_device="cuda", check_cache=True)
+
+
+def test_llama_128k_b8_fp8_hbm_values():
+    """The e5m2 configuration at 128K b8 with values in HBM, read in place (one 1 KB bulk copy
+    per chunk)."""
+    run_and_check(LLAMA_128K.with_(dtype="fp8", v_place="hbm"), 3, units=[4, 41], gen_device="cuda",
+                  check_cache=True, cache_units=[41])
