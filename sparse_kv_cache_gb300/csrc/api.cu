@@ -761,7 +761,7 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
         g.src = h->Vd; g.src_us = h->S * kD; g.list = h->miss_chunk; g.list_us = K; g.list_cap = K;
         g.cnt = h->miss_count; g.dst_idx = h->miss_slot; g.dst_cap = K; g.dst = h->Vc;
         g.dst_us = h->R * kD; g.nchunk = h->nchunk; g.es = h->es_v; g.U = U; g.err = h->err;
-        const int frc = launch_gather(g, (K + 7) / 8, ss);
+        const int frc = launch_fetch2(g, K, ss);
         if (frc) return SKV_ERR_CUDA;
         if (h->profiling) cudaEventRecord(ev[6], ss);
     }

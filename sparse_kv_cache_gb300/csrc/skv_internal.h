@@ -136,6 +136,8 @@ struct GatherParams {
     int* err;
 };
 int launch_gather(const GatherParams& p, int grid_x, cudaStream_t s);
+// the decode step's fetch, two chunks per warp (per-unit lists and counts required)
+int launch_fetch2(const GatherParams& p, int list_cap, cudaStream_t s);
 
 struct CompactParams {
     const float* Lfull; int64_t ncand;   // [U][ncand][d]
