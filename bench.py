@@ -523,7 +523,7 @@ def kernel_rooflines(w: Workload, M: int, st2: list, phase_ms: dict, phase_n: di
         ("select", "k_select_decode (softmax, group max, top-K, index scan, append)", "latency",
          U * w.n_selectable * G * 4),
         ("rebuild", "k_rebuild_tc (gather A rows, A.B, RoPE)", "hbm", misses * C * es * (r + d) + U * r * d * es),
-        ("fetch", "k_gather (value fetch)", "link" if host else "hbm", misses * C * d * es_v * (1 if host else 2)),
+        ("fetch", "k_gather2 (value fetch, two chunks per warp)", "link" if host else "hbm", misses * C * d * es_v * (1 if host else 2)),
         ("attn", "k_attn_tc + k_attn_merge (split-K attention)", "hbm",
          U * (rows_attn * d * (es + es_v) + 2 * G * d * es)),
     ]
