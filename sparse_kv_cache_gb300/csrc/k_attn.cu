@@ -488,10 +488,39 @@ __global__ void __launch_bounds__((kAWarps + 2) * 32, 1) k_attn_tc(const __grid_
 
     if (warp == 0) {
         // ---------------------------------------------------------------- producer warp
+        // The next segment's global reads (its cache slots' chunk ids, and the query rows when
+        // it starts a new unit) are issued one segment ahead, so that their round trips overlap
+        // the wait for a free stage and the current segment's copies.
         constexpr int QW = (G * 16 + 31) / 32;   // 16-byte words of the query rows per lane
         const uint64_t pol = l2_evict_first();   // read once per step
+        const int ncs = p.n_cache / kC;          // cache slots per unit
+        // chunk id of the cache slot lane `lane` copies for flat segment f (0: none)
+        auto load_vch = [&](int f) -> int {
+            if (!p.v_src || f >= f1) return 0;
+            const int uu = f / nsegu, s0 = (f - uu * nsegu) * kBSeg;
+            const int a0 = max(s0, p.n_out), a1 = min(s0 + min(kBSeg, ntot - s0), p.n_out + p.n_cache);
+            const int nv = a1 > a0 ? (a1 - a0) / kC : 0;
+            return lane < nv ? p.slot_chunk[static_cast<int64_t>(uu) * ncs + (a0 - p.n_out) / kC + lane] : 0;
+        };
+        auto load_q = [&](int uu, uint4 (&qw)[QW]) {
+#pragma unroll
+            for (int k = 0; k < QW; ++k) {
+                const int w = lane + 32 * k, n = w >> 4, c16 = w & 15;
+                qw[k] = n < G ? *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
+                                                                (static_cast<int64_t>(uu) * G + n) * kD + c16 * 8)
+                              : make_uint4(0, 0, 0, 0);
+            }
+        };
         int it = 0, u = f0 / nsegu, si = f0 - u * nsegu;
+        uint4 qcur[QW], qnxt[QW];
+#pragma unroll
+        for (int k = 0; k < QW; ++k) qcur[k] = qnxt[k] = make_uint4(0, 0, 0, 0);
+        if (f0 < f1) load_q(u, qcur);
+        int vch_cur = load_vch(f0);
         for (int f = f0; f < f1; ++f, ++it) {
+            const int vch_nxt = load_vch(f + 1);
+            const bool unext = f + 1 < f1 && si + 1 == nsegu;   // segment f + 1 starts a new unit
+            if (unext) load_q(u + 1, qnxt);
             const int st = it % S;
             const int okw = mbar_wait(&empty[st], ((it / S) & 1) ^ 1) ? 1 : 0;
             if (!__all_sync(0xffffffffu, okw)) {
@@ -512,7 +541,7 @@ __global__ void __launch_bounds__((kAWarps + 2) * 32, 1) k_attn_tc(const __grid_
             const int nvc = c1 > c0 ? (c1 - c0) / kC : 0;
             int vch = 0;
             if (lane < nvc) {
-                vch = p.slot_chunk[static_cast<int64_t>(ua) * (p.n_cache / kC) + (c0 - p.n_out) / kC + lane];
+                vch = vch_cur;
                 if (vch < 0 || vch >= p.nchunk) {
                     set_err(p.err, DEV_ERR_BOUNDS, 625);
                     vch = 0;   // read a valid chunk: the expected bytes still arrive
@@ -549,15 +578,17 @@ __global__ void __launch_bounds__((kAWarps + 2) * 32, 1) k_attn_tc(const __grid_
 #pragma unroll
             for (int k = 0; k < QW; ++k) {
                 const int w = lane + 32 * k, n = w >> 4, c16 = w & 15, kb = c16 >> 3, c = c16 & 7;
-                if (n < G) {
-                    const uint4 qw = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
-                                                                     (static_cast<int64_t>(ua) * G + n) * kD + c16 * 8);
-                    *reinterpret_cast<uint4*>(sQ + kb * 2048 + (n >> 3) * 1024 + (n & 7) * 128 + ((c ^ (n & 7)) << 4)) = qw;
-                }
+                if (n < G)
+                    *reinterpret_cast<uint4*>(sQ + kb * 2048 + (n >> 3) * 1024 + (n & 7) * 128 + ((c ^ (n & 7)) << 4)) = qcur[k];
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&full[st]);
+            vch_cur = vch_nxt;
+            if (unext) {
+#pragma unroll
+                for (int k = 0; k < QW; ++k) qcur[k] = qnxt[k];
+            }
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
