@@ -10,7 +10,11 @@
 //
 // One 1024-thread CTA per (batch, KV head) unit; a unit with more than 16K
 // chunks, when SMs are left over, runs on a thread-block cluster of up to 16
-// CTAs, each holding a contiguous slice of the unit's scores.  Ordering by
+// CTAs, each holding a contiguous slice of the unit's scores.  The one-CTA
+// form streams the unit's logits into two 64 KB shared-memory buffers by bulk
+// copies issued as soon as the scores are complete, in flight while the
+// log-sum-exp forms, so the score pass reads shared memory instead of waiting
+// on L2 round trips (22.1 -> 20.9 us per layer at 128K b8).  Ordering by
 // S2_j = max_g exp(z_gj - lse_g) equals ordering by v_j = max_g (z_gj - lse_g)
 // (exp is increasing), so the kernel ranks v_j.  The exact K-th largest value
 // T and the last index `jlast` taken among values equal to T are found with a
@@ -33,6 +37,7 @@
 namespace skv {
 
 constexpr int kBins = 2048;
+constexpr int kSelStageBytes = 65536;   // one logits buffer of the staged one-CTA form
 constexpr int kCand = 256;
 constexpr int kWarps = kSelThreads / 32;
 
@@ -514,6 +519,24 @@ __device__ __forceinline__ void select_decode(const SelectParams& p) {
     const int nlmax = (n + C - 1) / C;
     pdl_wait();      // the scores of this step
     pdl_trigger();
+    // staged one-CTA form: the unit's logits stream into two shared-memory buffers by bulk
+    // copies issued now, in flight while the log-sum-exp forms; the score pass reads them there
+    __shared__ uint64_t sbar[2];
+    const bool stg = !CL && p.stage;
+    const int sper = kSelStageBytes / (4 * G);             // scores per buffer
+    const int nstg = stg ? (nl + sper - 1) / sper : 0;
+    const float* z = p.logits + (static_cast<int64_t>(u) * n + j0) * G;   // this CTA's slice
+    auto issue = [&](int c) {   // buffer c & 1 <- scores [c * sper, min(nl, (c + 1) * sper))
+        const uint32_t bytes = static_cast<uint32_t>(min(sper, nl - c * sper)) * G * 4;
+        mbar_arrive_expect_tx(&sbar[c & 1], bytes);
+        bulk_g2s(dsm + p.stage_off + (c & 1) * kSelStageBytes, z + static_cast<int64_t>(c) * sper * G, bytes, &sbar[c & 1]);
+    };
+    if (stg && tid == 0) {
+        mbar_init(&sbar[0], 1);
+        mbar_init(&sbar[1], 1);
+        fence_mbar_init();
+        for (int c = 0; c < 2 && c < nstg; ++c) issue(c);
+    }
     float* vals = (nlmax <= p.smem_cap) ? reinterpret_cast<float*>(dsm) : p.vbuf + static_cast<int64_t>(u) * n + j0;
     const int cap_f = (nlmax <= p.smem_cap) ? ((nlmax + 3) & ~3) : 0;
     int32_t* sSel = reinterpret_cast<int32_t*>(dsm) + cap_f;
@@ -626,9 +649,36 @@ __device__ __forceinline__ void select_decode(const SelectParams& p) {
         }
         lse[g] = M + __logf(S);
     }
-    const float* z = p.logits + (static_cast<int64_t>(u) * n + j0) * G;   // this CTA's slice
     float lo = CUDART_INF_F, hi = -CUDART_INF_F;
-    if constexpr (G == 4) {
+    if (stg) {
+        bool ok = true;
+        for (int c = 0; c < nstg; ++c) {
+            const int b = c & 1;
+            if (ok && !mbar_wait(&sbar[b], (c >> 1) & 1)) {
+                if (tid == 0) set_err(p.err, DEV_ERR_TIMEOUT, 317);
+                (void)mbar_wait(&sbar[b], (c >> 1) & 1);   // the copy may still be in flight
+                ok = false;
+            }
+            const float* zs = reinterpret_cast<const float*>(dsm + p.stage_off + b * kSelStageBytes);
+            const int e0 = c * sper, e1 = min(nl, e0 + sper);
+            for (int j = e0 + tid; j < e1; j += kSelThreads) {
+                float v;
+                if constexpr (G == 4) {
+                    const float4 zz = reinterpret_cast<const float4*>(zs)[j - e0];
+                    v = fmaxf(fmaxf(zz.x - lse[0], zz.y - lse[1]), fmaxf(zz.z - lse[2], zz.w - lse[3]));
+                } else {
+                    v = -CUDART_INF_F;
+#pragma unroll
+                    for (int g = 0; g < G; ++g) v = fmaxf(v, zs[(j - e0) * G + g] - lse[g]);
+                }
+                vals[j] = v;
+                lo = fminf(lo, v);
+                hi = fmaxf(hi, v);
+            }
+            __syncthreads();   // buffer b is free again
+            if (tid == 0 && ok && c + 2 < nstg) issue(c + 2);
+        }
+    } else if constexpr (G == 4) {
         // four independent 16-byte loads in flight per thread
         const float4* z4 = reinterpret_cast<const float4*>(z);
         int j = tid;
@@ -863,10 +913,32 @@ int launch_select_decode(int dtype, const SelectParams& p, cudaStream_t s) {
     }
     const int nlmax = (p.n + C - 1) / C;
     const int cap_f = (nlmax <= p.smem_cap) ? ((nlmax + 3) & ~3) : 0;
-    const size_t smem = static_cast<size_t>(cap_f) * 4 + static_cast<size_t>(p.k) * 4 * 5;
+    size_t smem = static_cast<size_t>(cap_f) * 4 + static_cast<size_t>(p.k) * 4 * 5;
     if (C == 1) {
+        // the staged form when the scores live in shared memory, every buffer's bytes are whole
+        // 16-byte words and the two buffers fit beside them
+        SelectParams ps = p;
+        static int smem_room = -1;   // opt-in shared memory per block minus the kernel's static use
+        if (smem_room < 0) {
+            int dev = 0, optin = 0;
+            cudaFuncAttributes fa{};
+            if (cudaGetDevice(&dev) == cudaSuccess &&
+                cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess &&
+                cudaFuncGetAttributes(&fa, k_select_decode<8>) == cudaSuccess)
+                smem_room = optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
+            else
+                smem_room = 0;
+            cudaGetLastError();
+        }
+        const size_t off = (smem + 127) & ~size_t(127);
+        if (cap_f > 0 && (static_cast<int64_t>(p.n) * p.G * 4) % 16 == 0 &&
+            off + 2 * kSelStageBytes <= static_cast<size_t>(smem_room)) {
+            ps.stage = 1;
+            ps.stage_off = static_cast<int>(off);
+            smem = off + 2 * kSelStageBytes;
+        }
         cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (launch_pdl(fn, dim3(p.U), dim3(kSelThreads), smem, s, p) != cudaSuccess) {
+        if (launch_pdl(fn, dim3(p.U), dim3(kSelThreads), smem, s, ps) != cudaSuccess) {
             cudaGetLastError();
             return -1;
         }

@@ -81,6 +81,10 @@ struct SelectParams {
     const void* k_new; const void* v_new; void* k_loc; void* v_loc;
     int loc_cap; int64_t loc_pitch; int W; int es;   // local rows of unit u start at u * loc_pitch
     int es_v;             // bytes of a value element: 1 stores the new value in e5m2
+    // one-CTA decode form: the logits stream through two shared-memory buffers of
+    // kSelStageBytes by bulk copies (set by the launcher), starting at byte stage_off of the
+    // dynamic shared memory
+    int stage; int stage_off;
     int* err;
 };
 int launch_select_decode(int dtype, const SelectParams& p, cudaStream_t s);
