@@ -22,8 +22,27 @@
 #include <vector>
 
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "shadowkv.h"
 #include "skv_internal.h"
+
+namespace {
+// An NVTX range on the host timeline: one per library call and one per decode phase, so that a
+// profiler shows where a step's launches come from and ncu can select a phase's kernels
+// (--nvtx --nvtx-include).  A push and a pop cost a few nanoseconds when no tool listens.
+struct NvtxRange {
+    bool on = true;
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    void end() {
+        if (on) nvtxRangePop();
+        on = false;
+    }
+    ~NvtxRange() { end(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
+}  // namespace
 
 using namespace skv;
 
@@ -406,6 +425,7 @@ int shadowkv_prefill_index(const skv_config* cfg, const void* A, const void* B, 
 
 int shadowkv_prefill_index_keys(const skv_config* cfg, const void* A, const void* B, const void* Kx, const void* V,
                                 skv_stream stream, skv_layer** out) {
+    NvtxRange call("shadowkv_prefill_index");
     if (!out) return SKV_ERR_INVALID;
     *out = nullptr;
     int rc = shadowkv_validate_config(cfg);
@@ -678,6 +698,7 @@ int shadowkv_prefill_index_keys(const skv_config* cfg, const void* A, const void
 
 int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const void* v_new, void* out,
                          int32_t* sel_out, skv_stream main, skv_stream side) {
+    NvtxRange call("shadowkv_decode_step");
     if (!h || !q || !k_new || !v_new || !out) return SKV_ERR_INVALID;
     if (h->t >= h->Tmax) return SKV_ERR_STEP_LIMIT;
     if (h->v_huge && h->t == 0) {
@@ -718,6 +739,7 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
         pp.a_rows = h->Tpad; pp.pos = h->S + t; pp.loc_pitch = h->R; pp.loc_row = h->W + t;
         if (launch_plus_append(h->dtype == SKV_F32 ? 0 : 1, pp, U / h->H, ss)) return SKV_ERR_CUDA;
     }
+    NvtxRange ph_score("a2 landmark scoring");
     // a2: landmark scoring
     ScoreParams sp{};
     sp.L = h->L; sp.q = q; sp.logits = h->logits; sp.part = h->score_part; sp.n_c = h->n_c;
@@ -727,6 +749,8 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     if (h->dtype == SKV_FP8 && launch_qsplit(q, h->qt, h->qinv, U, G, sm)) return SKV_ERR_CUDA;
     if (launch_score(h->dtype, G, &h->tmL, sp, h->score_ncta, sm)) return SKV_ERR_CUDA;
     if (h->profiling) cudaEventRecord(ev[1], sm);
+    ph_score.end();
+    NvtxRange ph_select("a3-a4 selection, index scan, append");
     // a3 + a4 + a1: top-K, index scan, append
     SelectParams sel{};
     sel.n = h->n_c; sel.k = K; sel.U = U; sel.H = h->H; sel.G = G;
@@ -747,6 +771,8 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
         return SKV_ERR_CUDA;
     }
     if (h->profiling) cudaEventRecord(ev[2], sm);
+    ph_select.end();
+    NvtxRange ph_fetch("a6 value fetch");
     // a6 on the side stream: value rows of the missed chunks into their slots.  With values in
     // HBM on the tensor-core path there is nothing to move: attention reads them in V.
     // side_pending: the side stream holds work attention must wait for
@@ -770,6 +796,8 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     // it before the rebuild, so that the attention still follows the rebuild directly
     const bool wait_early = side_pending && h->v_direct;
     if (wait_early) cudaStreamWaitEvent(sm, h->ev_fetch, 0);
+    ph_fetch.end();
+    NvtxRange ph_rebuild("a5 key rebuild");
     // a5 on the main stream: rebuild + RoPE of the missed chunks' keys (timed from its own
     // launch, which with a single stream comes after the fetch)
     if (h->profiling) cudaEventRecord(ev[7], sm);
@@ -783,7 +811,9 @@ int shadowkv_decode_step(skv_layer* h, const void* q, const void* k_new, const v
     if (rc) return SKV_ERR_CUDA;
     if (h->profiling) cudaEventRecord(ev[3], sm);
     if (side_pending && !wait_early) cudaStreamWaitEvent(sm, h->ev_fetch, 0);
-    // a7: attention over outliers + cache + local, split-K with an in-kernel merge
+    ph_rebuild.end();
+    NvtxRange ph_attn("a7 sparse attention");
+    // a7: attention over outliers + cache + local, split-K with a dependent merge kernel
     AttnParams ap{};
     ap.q = q; ap.k_out = h->Kout; ap.v_out = h->Vout; ap.n_out = h->O * kC;
     ap.k_c = h->Kc; ap.v_c = h->Vc; ap.n_cache = K * kC;
