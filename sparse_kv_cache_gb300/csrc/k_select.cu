@@ -10,11 +10,12 @@
 //
 // One 1024-thread CTA per (batch, KV head) unit; a unit with more than 16K
 // chunks, when SMs are left over, runs on a thread-block cluster of up to 16
-// CTAs, each holding a contiguous slice of the unit's scores.  The one-CTA
-// form streams the unit's logits into two 64 KB shared-memory buffers by bulk
-// copies issued as soon as the scores are complete, in flight while the
-// log-sum-exp forms, so the score pass reads shared memory instead of waiting
-// on L2 round trips (22.1 -> 20.9 us per layer at 128K b8).  Ordering by
+// CTAs, each holding a contiguous slice of the unit's scores.  Each CTA
+// streams its logits into two 64 KB shared-memory buffers by bulk copies
+// issued as soon as the scores are complete, in flight while the log-sum-exp
+// forms, so the score pass reads shared memory instead of waiting on L2 round
+// trips (22.1 -> 20.9 us per layer at 128K b8; the cluster form at 1M b1:
+// 245.7 -> 247.6 tokens/s).  Ordering by
 // S2_j = max_g exp(z_gj - lse_g) equals ordering by v_j = max_g (z_gj - lse_g)
 // (exp is increasing), so the kernel ranks v_j.  The exact K-th largest value
 // T and the last index `jlast` taken among values equal to T are found with a
@@ -522,7 +523,7 @@ __device__ __forceinline__ void select_decode(const SelectParams& p) {
     // staged one-CTA form: the unit's logits stream into two shared-memory buffers by bulk
     // copies issued now, in flight while the log-sum-exp forms; the score pass reads them there
     __shared__ uint64_t sbar[2];
-    const bool stg = !CL && p.stage;
+    const bool stg = p.stage;
     const int sper = kSelStageBytes / (4 * G);             // scores per buffer
     const int nstg = stg ? (nl + sper - 1) / sper : 0;
     const float* z = p.logits + (static_cast<int64_t>(u) * n + j0) * G;   // this CTA's slice
@@ -914,28 +915,30 @@ int launch_select_decode(int dtype, const SelectParams& p, cudaStream_t s) {
     const int nlmax = (p.n + C - 1) / C;
     const int cap_f = (nlmax <= p.smem_cap) ? ((nlmax + 3) & ~3) : 0;
     size_t smem = static_cast<size_t>(cap_f) * 4 + static_cast<size_t>(p.k) * 4 * 5;
+    // the staged form when the scores live in shared memory, every CTA's slice and buffer starts
+    // on a 16-byte boundary, and the two buffers fit beside the scores
+    static int smem_room = -1;   // opt-in shared memory per block minus the kernels' static use
+    if (smem_room < 0) {
+        int dev = 0, optin = 0;
+        cudaFuncAttributes fa{}, fc{};
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess &&
+            cudaFuncGetAttributes(&fa, k_select_decode<8>) == cudaSuccess &&
+            cudaFuncGetAttributes(&fc, k_select_decode_cl<8>) == cudaSuccess)
+            smem_room = optin - static_cast<int>(std::max(fa.sharedSizeBytes, fc.sharedSizeBytes)) - 1024;
+        else
+            smem_room = 0;
+        cudaGetLastError();
+    }
+    const size_t off = (smem + 127) & ~size_t(127);
+    const bool aligned = C == 1 ? (static_cast<int64_t>(p.n) * p.G * 4) % 16 == 0 : (p.G * 4) % 16 == 0;
+    const bool staged = cap_f > 0 && aligned && off + 2 * kSelStageBytes <= static_cast<size_t>(smem_room);
+    if (staged) smem = off + 2 * kSelStageBytes;
     if (C == 1) {
-        // the staged form when the scores live in shared memory, every buffer's bytes are whole
-        // 16-byte words and the two buffers fit beside them
         SelectParams ps = p;
-        static int smem_room = -1;   // opt-in shared memory per block minus the kernel's static use
-        if (smem_room < 0) {
-            int dev = 0, optin = 0;
-            cudaFuncAttributes fa{};
-            if (cudaGetDevice(&dev) == cudaSuccess &&
-                cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess &&
-                cudaFuncGetAttributes(&fa, k_select_decode<8>) == cudaSuccess)
-                smem_room = optin - static_cast<int>(fa.sharedSizeBytes) - 1024;
-            else
-                smem_room = 0;
-            cudaGetLastError();
-        }
-        const size_t off = (smem + 127) & ~size_t(127);
-        if (cap_f > 0 && (static_cast<int64_t>(p.n) * p.G * 4) % 16 == 0 &&
-            off + 2 * kSelStageBytes <= static_cast<size_t>(smem_room)) {
+        if (staged) {
             ps.stage = 1;
             ps.stage_off = static_cast<int>(off);
-            smem = off + 2 * kSelStageBytes;
         }
         cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (launch_pdl(fn, dim3(p.U), dim3(kSelThreads), smem, s, ps) != cudaSuccess) {
@@ -946,6 +949,10 @@ int launch_select_decode(int dtype, const SelectParams& p, cudaStream_t s) {
     }
     SelectParams pc = p;
     pc.cluster = C;
+    if (staged) {
+        pc.stage = 1;
+        pc.stage_off = static_cast<int>(off);
+    }
     cudaFuncSetAttribute(fnc, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.U * C);
