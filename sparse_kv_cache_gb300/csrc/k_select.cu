@@ -15,7 +15,9 @@
 // issued as soon as the scores are complete, in flight while the log-sum-exp
 // forms, so the score pass reads shared memory instead of waiting on L2 round
 // trips (22.1 -> 20.9 us per layer at 128K b8; the cluster form at 1M b1:
-// 245.7 -> 247.6 tokens/s).  Ordering by
+// 245.7 -> 247.6 tokens/s).  The one-CTA form then brings the unit's position ->
+// chunk id table into the first buffer the same way, in flight through the
+// threshold and the compaction (2388 -> 2400 tokens/s at 128K b8, values in HBM).  Ordering by
 // S2_j = max_g exp(z_gj - lse_g) equals ordering by v_j = max_g (z_gj - lse_g)
 // (exp is increasing), so the kernel ranks v_j.  The exact K-th largest value
 // T and the last index `jlast` taken among values equal to T are found with a
@@ -526,6 +528,7 @@ __device__ __forceinline__ void select_decode(const SelectParams& p) {
     const bool stg = p.stage;
     const int sper = kSelStageBytes / (4 * G);             // scores per buffer
     const int nstg = stg ? (nl + sper - 1) / sper : 0;
+    const bool ids_stg = !CL && stg && n % 4 == 0 && n * 4 <= kSelStageBytes;
     const float* z = p.logits + (static_cast<int64_t>(u) * n + j0) * G;   // this CTA's slice
     auto issue = [&](int c) {   // buffer c & 1 <- scores [c * sper, min(nl, (c + 1) * sper))
         const uint32_t bytes = static_cast<uint32_t>(min(sper, nl - c * sper)) * G * 4;
@@ -679,6 +682,12 @@ __device__ __forceinline__ void select_decode(const SelectParams& p) {
             __syncthreads();   // buffer b is free again
             if (tid == 0 && ok && c + 2 < nstg) issue(c + 2);
         }
+        // one-CTA form: the unit's position -> chunk id table, into buffer 0 once the scores are
+        // read, in flight through the threshold and the compaction
+        if (tid == 0 && ids_stg) {
+            mbar_arrive_expect_tx(&sbar[0], static_cast<uint32_t>(n) * 4);
+            bulk_g2s(dsm + p.stage_off, p.ids + static_cast<int64_t>(u) * n, static_cast<uint32_t>(n) * 4, &sbar[0]);
+        }
     } else if constexpr (G == 4) {
         // four independent 16-byte loads in flight per thread
         const float4* z4 = reinterpret_cast<const float4*>(z);
@@ -729,8 +738,18 @@ __device__ __forceinline__ void select_decode(const SelectParams& p) {
             for (int i = tid; i < K; i += kSelThreads) sSel[i] = i;
             __syncthreads();
         }
-        // positions -> original chunk ids, every load in flight at once
-        for (int i = tid; i < K; i += kSelThreads) sSel[i] = ids[sSel[i]];
+        // positions -> original chunk ids, from the staged table or with every load in flight
+        if (ids_stg) {
+            const uint32_t par = static_cast<uint32_t>((nstg + 1) / 2) & 1u;   // buffer 0's next phase
+            if (!mbar_wait(&sbar[0], par)) {
+                if (tid == 0) set_err(p.err, DEV_ERR_TIMEOUT, 318);
+                (void)mbar_wait(&sbar[0], par);
+            }
+            const int32_t* sids = reinterpret_cast<const int32_t*>(dsm + p.stage_off);
+            for (int i = tid; i < K; i += kSelThreads) sSel[i] = sids[sSel[i]];
+        } else {
+            for (int i = tid; i < K; i += kSelThreads) sSel[i] = ids[sSel[i]];
+        }
         __syncthreads();
     } else {
         // each CTA translates its slice's picks, then places them after the lower ranks' picks
