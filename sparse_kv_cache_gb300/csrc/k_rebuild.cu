@@ -266,11 +266,17 @@ __global__ void __launch_bounds__(128, 1) k_rebuild_tc(const __grid_constant__ C
     const uint32_t tmem = tmem_slot;
     const int b = u / p.H;
 
-    // A rows: one issuing thread per chunk (its nkb 64-column boxes of 8 rows)
-    if (tid < nch && ti[tid].chunk >= 0)
-        for (int kb = 0; kb < nkb; ++kb)
-            tma_load_2d(sA + kb * 16384 + tid * 1024, &tmA, kb * 64,
-                        static_cast<int>(b * p.S + static_cast<int64_t>(ti[tid].chunk) * kC), &bar_tma);
+    // A rows: the tile's nch x nkb boxes (8 rows x 64 columns of one chunk) spread over lanes
+    // 0-15 of the four warps, one box per thread at a time: the copy instructions of different
+    // warps issue side by side (measured: 21.1 against 22.7 us per layer at 128K b8 for one
+    // thread per chunk issuing its nkb boxes)
+    if ((tid & 31) < 16)
+        for (int o = warp * 16 + (tid & 31); o < nch * nkb; o += 64) {
+            const int c = o / nkb, kb = o - c * nkb;
+            if (ti[c].chunk >= 0)
+                tma_load_2d(sA + kb * 16384 + c * 1024, &tmA, kb * 64,
+                            static_cast<int>(b * p.S + static_cast<int64_t>(ti[c].chunk) * kC), &bar_tma);
+        }
     if (tid == 0) {
         int nvalid = 0;
         for (int c = 0; c < nch; ++c) nvalid += ti[c].chunk >= 0;
