@@ -79,6 +79,13 @@ def test_group_sizes(G):
     run_and_check(TINY.with_(n_q_heads=2 * G, seed=20 + G), 3)
 
 
+@pytest.mark.parametrize("G,dtype", [(1, "f32"), (2, "bf16")])
+def test_selection_reads_unstaged_scores(G, dtype):
+    # n_c = 505 selectable chunks: a unit's scores are not whole 16-byte words for G < 4, so the
+    # selection reads them straight from global memory instead of staging them in shared memory
+    run_and_check(TINY.with_(seq_len=4096 + 8, n_q_heads=2 * G, dtype=dtype, seed=40 + G), 3)
+
+
 @pytest.mark.parametrize("rank", [8, 256])
 def test_rank_extremes_bf16(rank):
     run_and_check(SMALL_BF16.with_(rank=rank, batch=1, seed=30 + rank), 3)
