@@ -79,6 +79,15 @@ def test_group_sizes(G):
     run_and_check(TINY.with_(n_q_heads=2 * G, seed=20 + G), 3)
 
 
+def test_merge_of_many_contributors():
+    # one unit whose attention spans ~67 CTAs: more partial records than the merge stages in
+    # shared memory (96 KB, 46 contributors at G = 4), so they are loaded directly
+    w = Workload(name="merge-many", layers=1, batch=1, seq_len=32768, n_kv_heads=1, n_q_heads=4,
+                 head_dim=128, rank=160, chunk=8, n_select=1024, n_outlier=16, local_window=32, steps=2,
+                 dtype="bf16", v_place="hbm", drift=0.9, seed=51)
+    run_and_check(w, 2)
+
+
 @pytest.mark.parametrize("G,dtype", [(1, "f32"), (2, "bf16")])
 def test_selection_reads_unstaged_scores(G, dtype):
     # n_c = 505 selectable chunks: a unit's scores are not whole 16-byte words for G < 4, so the
