@@ -859,13 +859,14 @@ __global__ void __launch_bounds__(kD) k_attn_merge(AttnParams p, int ncta, int s
     for (int g = 0; g < G; ++g) { M[g] = -CUDART_INF_F; L[g] = 0.f; A[g] = 0.f; }
     if (stg) {
         constexpr uint32_t kBytes = G * kPartPitch * 4;   // one contributor's partial
-        if (dim == 0) {
-            mbar_arrive_expect_tx(&mbar, static_cast<uint32_t>(ncon) * kBytes);
-            for (int c = 0; c < ncon; ++c) {
+        // one arrival with the byte count; the copies issued by lanes 0-7 of the four warps, so
+        // that different warps' copy instructions issue side by side
+        if (dim == 0) mbar_arrive_expect_tx(&mbar, static_cast<uint32_t>(ncon) * kBytes);
+        if ((dim & 31) < 8)
+            for (int c = (dim >> 5) * 8 + (dim & 31); c < ncon; c += 32) {
                 const int st = aseg_start(cA + c, F, ncta) - u * nsegu;
                 bulk_g2s(msm + c * kBytes, parts + static_cast<int64_t>(st > 0 ? st : 0) * G * kPartPitch, kBytes, &mbar);
             }
-        }
         if (!mbar_wait(&mbar, 0)) {
             if (dim == 0) set_err(p.err, DEV_ERR_TIMEOUT, 631);
             (void)mbar_wait(&mbar, 0);
